@@ -1,0 +1,529 @@
+#!/usr/bin/env python3
+"""Benchmark of chunked-prefill extend attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg5] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of synthetic input:
+  cfg1/2/3/5  the whole chunked prefill of one request: the chunk plan, then
+              for every chunk the KV append and the extend attention;
+  cfg4        one mixed step: the mixed-step plan, the KV append, the
+              split-KV decode rows and the prefill chunk.
+Default workload: cfg5 (N=131072, C=1024, 128 chunks, GQA 64/8, d=128, bf16),
+the long-context configuration whose per-chunk TFLOP/s the metric tracks.
+
+Rank 0 prints one JSON line.  ``value`` is algorithmic TFLOP/s over all ranks
+(4*d*H_q*(E*P + E(E+1)/2) per chunk, plus 4*d*H_q*L per decode row);
+``roofline`` describes the dominant kernel; ``cpu_baseline`` times the float64
+oracle on a bounded sample; ``e2e`` repeats the measurement with host inputs
+and outputs copied inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_prefill_extend_gb300 import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sustained": p["bf16_tflops_sustained"],
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def chunk_flops(d, h_q, P, E):
+    return 4.0 * d * h_q * (E * P + E * (E + 1) / 2.0)
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Chunked:
+    """Whole chunked prefill of one request (cfg1/2/3/5)."""
+
+    def __init__(self, spec, device, cpe):
+        self.spec, self.cpe, self.device = spec, cpe, device
+        self.req = W.make_chunked(spec, device=device)
+        self.chunks, self.cached, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+        self.idx = {c.index: (torch.tensor([0, c.query_len], dtype=torch.int32, device=device),
+                              torch.tensor([c.prefix_len], dtype=torch.int32, device=device)) for c in self.chunks}
+        self.out = torch.empty_like(self.req.q)
+        self.ws = cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, device)
+        self.flops = sum(chunk_flops(spec.d, spec.h_q, c.prefix_len, c.query_len) for c in self.chunks)
+        self.tokens = sum(c.query_len for c in self.chunks)
+        self.in_bytes = sum(t.numel() * t.element_size() for t in (self.req.q, self.req.k, self.req.v))
+        self.kernel = "extend_tc_kernel" if spec.dtype == torch.bfloat16 else "extend_simt_kernel"
+        self.bound = "tensor"
+        self.small = self.in_bytes + 2 * self.req.k_cache.numel() * self.req.k_cache.element_size() < 2 * L2_BYTES
+
+    def step(self, ev=None, q=None, k=None, v=None, out=None):
+        cpe, req = self.cpe, self.req
+        q = req.q if q is None else q
+        k = req.k if k is None else k
+        v = req.v if v is None else v
+        out = self.out if out is None else out
+        chunks, _, _ = cpe.cpe_plan_chunks(self.spec.input_len, self.spec.hit_rate, self.spec.chunk)
+        for c in chunks:
+            qo, pl = self.idx[c.index]
+            a = c.prefix_len - self.cached
+            cpe.cpe_kv_append(k[a:a + c.query_len], v[a:a + c.query_len], req.k_cache, req.v_cache,
+                              req.page_table, qo, pl)
+            if ev is not None:
+                ev[0].append(torch.cuda.Event(enable_timing=True))
+                ev[0][-1].record()
+            cpe.cpe_extend_attention(q[a:a + c.query_len], req.k_cache, req.v_cache, req.page_table, qo, pl,
+                                     c.seq_len, out=out[a:a + c.query_len], workspace=self.ws)
+            if ev is not None:
+                ev[1].append(torch.cuda.Event(enable_timing=True))
+                ev[1][-1].record()
+        return out
+
+    def host_io(self):
+        return [self.req.q, self.req.k, self.req.v], self.out
+
+    def kernel_units(self):
+        return self.flops / len(self.chunks), "flop"
+
+    def oracle_sample(self, oracle, budget_s):
+        """Time the oracle on sampled rows of sampled chunks; returns (flops, seconds, text)."""
+        spec, req = self.spec, self.req
+        kc, vc = req.k_cache.cpu(), req.v_cache.cpu()
+        pt = torch.tensor([req.page_table_host], dtype=torch.int32)
+        picks = sorted(set([0, len(self.chunks) // 2, len(self.chunks) - 1]))
+        flops = 0.0
+        t0 = time.perf_counter()
+        n_rows = 0
+        rows_per = 4
+        while True:
+            for t in picks:
+                c = self.chunks[t]
+                a = c.prefix_len - self.cached
+                rows = W.sample_rows(c.query_len, 32, rows_per, 7 + t)
+                q = req.q[a:a + c.query_len].cpu()
+                oracle.extend_attention(q, kc, vc, pt, [0, c.query_len], [c.prefix_len], spec.h_q, spec.h_kv,
+                                        rows=rows)
+                for r in rows:
+                    flops += 4.0 * spec.d * spec.h_q * (c.prefix_len + r + 1)
+                n_rows += len(rows)
+            if time.perf_counter() - t0 > budget_s * 0.3 or rows_per >= 256:
+                break
+            rows_per *= 2
+        dt = time.perf_counter() - t0
+        return flops, dt, f"{n_rows} query rows x {spec.h_q} heads from chunks {picks} (all keys of each row)"
+
+
+class Mixed:
+    """One mixed step (cfg4)."""
+
+    def __init__(self, spec, device, cpe):
+        self.spec, self.cpe, self.device = spec, cpe, device
+        g = torch.Generator().manual_seed(spec.seed)
+        ctx = torch.randint(spec.ctx_lo, spec.ctx_hi + 1, (spec.n_decode,), generator=g).tolist()
+        plan = cpe.cpe_plan_mixed_step(spec.token_budget, ctx, spec.prefill_prefix, spec.prefill_remaining)
+        self.mb = W.make_mixed(spec, plan["extend_len"], device=device)
+        self.plan = cpe.cpe_plan_mixed_step(spec.token_budget, self.mb.ctx_len, spec.prefill_prefix,
+                                            spec.prefill_remaining)
+        self.qo = torch.tensor(self.plan["qo_indptr"], dtype=torch.int32, device=device)
+        self.pl = torch.tensor(self.plan["prefix_len"], dtype=torch.int32, device=device)
+        self.max_kv = max(self.plan["kv_len"])
+        n = len(self.plan["prefix_len"])
+        self.ws = cpe.alloc_workspace(n, self.mb.q.shape[0], spec.h_q, spec.h_kv, spec.d, self.max_kv, device)
+        self.out = torch.empty_like(self.mb.q)
+        E, P = self.plan["extend_len"], spec.prefill_prefix
+        dec_L = self.plan["kv_len"][:self.plan["n_decode"]]
+        self.flops = chunk_flops(spec.d, spec.h_q, P, E) + sum(4.0 * spec.d * spec.h_q * L for L in dec_L)
+        self.decode_bytes = sum(2.0 * L * spec.h_kv * spec.d * 2 + 2.0 * spec.h_q * spec.d * 2 for L in dec_L)
+        self.tokens = E + self.plan["n_decode"]
+        self.in_bytes = sum(t.numel() * t.element_size() for t in (self.mb.q, self.mb.k_new, self.mb.v_new))
+        self.kernel = "decode_kernel"
+        self.bound = "hbm"
+        self.small = False
+
+    def step(self, ev=None, q=None, k=None, v=None, out=None):
+        cpe, mb, spec = self.cpe, self.mb, self.spec
+        q = mb.q if q is None else q
+        k = mb.k_new if k is None else k
+        v = mb.v_new if v is None else v
+        out = self.out if out is None else out
+        cpe.cpe_plan_mixed_step(spec.token_budget, mb.ctx_len, spec.prefill_prefix, spec.prefill_remaining)
+        cpe.cpe_mixed_step(q, k, v, mb.k_cache, mb.v_cache, mb.page_table, self.qo, self.pl, self.plan["n_decode"],
+                           self.max_kv, out=out, workspace=self.ws)
+        return out
+
+    def decode_only(self, ev):
+        """The decode rows alone through cpe_decode_attention (for the HBM roofline)."""
+        nd = self.plan["n_decode"]
+        ev[0].append(torch.cuda.Event(enable_timing=True))
+        ev[0][-1].record()
+        self.cpe.cpe_decode_attention(self.mb.q[:nd], self.mb.k_cache, self.mb.v_cache, self.mb.page_table[:nd],
+                                      self.pl[:nd], self.max_kv, out=self.out[:nd], workspace=self.ws)
+        ev[1].append(torch.cuda.Event(enable_timing=True))
+        ev[1][-1].record()
+
+    def host_io(self):
+        return [self.mb.q, self.mb.k_new, self.mb.v_new], self.out
+
+    def oracle_sample(self, oracle, budget_s):
+        spec, mb, plan = self.spec, self.mb, self.plan
+        t0 = time.perf_counter()
+        flops = 0.0
+        picks = list(range(0, plan["n_decode"], max(1, plan["n_decode"] // 8)))[:8]
+        kl = [plan["kv_len"][s] for s in picks]
+        pg = mb.k_cache.shape[1]
+        need = [-(-L // pg) for L in kl]
+        ids = torch.cat([mb.page_table_host[s, :n].long() for s, n in zip(picks, need)])
+        kc, vc = mb.k_cache[ids.to(mb.k_cache.device)].cpu(), mb.v_cache[ids.to(mb.v_cache.device)].cpu()
+        pt = torch.full((len(picks), max(need)), -1, dtype=torch.int32)
+        off = 0
+        for r, n in enumerate(need):
+            pt[r, :n] = torch.arange(off, off + n, dtype=torch.int32)
+            off += n
+        t0 = time.perf_counter()
+        oracle.extend_attention(mb.q[picks].cpu(), kc, vc, pt, list(range(len(picks) + 1)),
+                                [plan["prefix_len"][s] for s in picks], spec.h_q, spec.h_kv)
+        flops += sum(4.0 * spec.d * spec.h_q * L for L in kl)
+        dt = time.perf_counter() - t0
+        return flops, dt, f"{len(picks)} decode rows x {spec.h_q} heads (all keys)"
+
+
+def make_workload(name, device, cpe):
+    spec = W.CONFIGS[name]
+    return Mixed(spec, device, cpe) if isinstance(spec, W.MixedSpec) else Chunked(spec, device, cpe)
+
+
+# --------------------------------------------------------------------------- helpers
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_ours(args, ws, rank, local):
+    from chunked_prefill_extend_gb300 import cpe
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks = _peaks()
+    wl = make_workload(args.workload, device, cpe)
+    flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if wl.small else None
+    for _ in range(args.warmup):
+        wl.step()
+        if flush is not None:
+            flush_l2(flush)
+    st, detail = cpe.cpe_get_device_status()
+    if st != cpe.CPE_OK:
+        raise RuntimeError(f"device status after warm-up: {cpe.cpe_status_string(st)} ({detail})")
+
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    kev = ([], [])
+    sev = []
+    launches0 = cpe.cpe_launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        wl.step(ev=kev)
+        b.record()
+        sev.append((a, b))
+        if flush is not None:
+            flush_l2(flush)
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = cpe.cpe_launch_count() - launches0
+    clk = clocks.stop()
+    st, detail = cpe.cpe_get_device_status()
+    if st != cpe.CPE_OK:
+        raise RuntimeError(f"device status after timing: {cpe.cpe_status_string(st)} ({detail})")
+    step_ms = [a.elapsed_time(b) for a, b in sev]
+    region_ms = t_start.elapsed_time(t_end)
+    my_ms = sum(step_ms) if flush is not None else region_ms
+    total_ms = max_over_ranks(my_ms, ws, device)
+    ms_per_step = total_ms / args.steps
+    value = wl.flops * ws / (ms_per_step * 1e-3) / 1e12
+
+    # dominant kernel, timed live with events on the launching stream
+    if isinstance(wl, Mixed):
+        dev_ev = ([], [])
+        for _ in range(max(3, args.steps // 2)):
+            wl.decode_only(dev_ev)
+        torch.cuda.synchronize()
+        kms = statistics.mean(a.elapsed_time(b) for a, b in zip(*dev_ev))
+        achieved = wl.decode_bytes / (kms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "decode_kernel (+ merge)",
+                "peak_source": peaks["source"] + " hbm_gbs", "units_per_launch": wl.decode_bytes}
+    else:
+        kms_list = [a.elapsed_time(b) for a, b in zip(*kev)]
+        kms = statistics.mean(kms_list)
+        per_launch = wl.flops / len(wl.chunks)
+        achieved = per_launch / (kms * 1e-3) / 1e12
+        pk = peaks["bf16_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "traffic": None, "kernel": "extend attention call (schedule_kernel + extend_tc_kernel)",
+                "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": per_launch}
+        last = kms_list[-len(wl.chunks):]
+        curve = [(c.prefix_len, chunk_flops(wl.spec.d, wl.spec.h_q, c.prefix_len, c.query_len) / (t * 1e-3) / 1e12)
+                 for c, t in zip(wl.chunks, last)]
+        pick = sorted(set([0, len(curve) // 4, len(curve) // 2, 3 * len(curve) // 4, len(curve) - 1]))
+        roof["per_chunk_tflops"] = {str(curve[i][0]): round(curve[i][1], 1) for i in pick}
+
+    # end to end through the public API with host buffers
+    e2e = e2e_measure(wl, args, device, ws)
+
+    line = {
+        "metric": "extend-attn TFLOP/s & tokens/s per chunk; % bf16 TC peak / % HBM BW (1 GB300)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if W.CONFIGS[args.workload].dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "tokens_per_s": wl.tokens * ws / (ms_per_step * 1e-3),
+        "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}",
+                   "l2": "flushed between steps (256 MiB write outside the per-step events)" if flush is not None
+                   else "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{ws}", "flops_per_step": wl.flops},
+        "roofline": roof, "clocks": clk, "gpu_launches": launches, "e2e": e2e,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_measure(wl, args, device, ws):
+    """The same metric through the public API with pinned host inputs copied in
+    and the output copied back inside the timed region."""
+    ins, out_dev = wl.host_io()
+    host_in = [t.cpu().pin_memory() for t in ins]
+    host_out = torch.empty(out_dev.shape, dtype=out_dev.dtype, pin_memory=True)
+    dev_in = [torch.empty_like(t) for t in ins]
+    dev_out = torch.empty_like(out_dev)
+    n = max(3, min(args.steps, 10))
+    for _ in range(2):
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        wl.step(q=dev_in[0], k=dev_in[1], v=dev_in[2], out=dev_out)
+        host_out.copy_(dev_out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        wl.step(q=dev_in[0], k=dev_in[1], v=dev_in[2], out=dev_out)
+        host_out.copy_(dev_out, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / n, ws, device)
+    return {"value": wl.flops * ws / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+            "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": ms}
+
+
+def cpu_baseline(wl, args):
+    import oracle
+    oracle.build()
+    flops, dt, text = wl.oracle_sample(oracle, budget_s=20.0)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": text, "seconds": dt}
+
+
+def run_reference(args, ws, rank, local):
+    """The oracle (float64 CPU) as the reference arm, on a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    spec = W.CONFIGS[args.workload]
+    # inputs generated on the CPU with the same seeded recipe (no GPU needed)
+    if isinstance(spec, W.MixedSpec):
+        wl = _ref_mixed(spec)
+    else:
+        wl = _ref_chunked(spec)
+    for _ in range(args.warmup):
+        wl()
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += wl()
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    line = {"metric": "extend-attn TFLOP/s & tokens/s per chunk; % bf16 TC peak / % HBM BW (1 GB300)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": wl.text},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _ref_chunked(spec):
+    import oracle
+    # the sample: 2 query rows (all heads, all keys) from each of three chunks
+    chunks = oracle.plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+    picks = sorted(set([0, len(chunks) // 2, len(chunks) - 1]))
+    g = torch.Generator().manual_seed(spec.seed)
+    N = spec.input_len
+    pg = spec.page_size
+    npages = -(-N // pg)
+    kc = (torch.randn(npages, pg, spec.h_kv, spec.d, generator=g) * spec.std).to(spec.dtype)
+    vc = (torch.randn(npages, pg, spec.h_kv, spec.d, generator=g) * spec.std).to(spec.dtype)
+    pt = torch.arange(npages, dtype=torch.int32).view(1, -1)
+    state = {"k": 0}
+
+    def step():
+        fl = 0.0
+        for t in picks:
+            c = chunks[t]
+            q = (torch.randn(c.query_len, spec.h_q, spec.d, generator=g) * spec.std).to(spec.dtype)
+            rows = [c.query_len - 1 - ((state["k"] * 7 + 3 * j) % c.query_len) for j in range(2)]
+            oracle.extend_attention(q, kc, vc, pt, [0, c.query_len], [c.prefix_len], spec.h_q, spec.h_kv, rows=rows)
+            fl += sum(4.0 * spec.d * spec.h_q * (c.prefix_len + r + 1) for r in rows)
+        state["k"] += 1
+        return fl
+    step.text = f"2 query rows x {spec.h_q} heads from chunks {picks} per step (all keys of each row)"
+    return step
+
+
+def _ref_mixed(spec):
+    import oracle
+    g = torch.Generator().manual_seed(spec.seed)
+    ctx = torch.randint(spec.ctx_lo, spec.ctx_hi + 1, (spec.n_decode,), generator=g).tolist()
+    pg = spec.page_size
+    picks = ctx[:4]
+    npg = [-(-L // pg) for L in picks]
+    kc = (torch.randn(sum(npg), pg, spec.h_kv, spec.d, generator=g) * spec.std).to(spec.dtype)
+    vc = (torch.randn(sum(npg), pg, spec.h_kv, spec.d, generator=g) * spec.std).to(spec.dtype)
+    pt = torch.full((len(picks), max(npg)), -1, dtype=torch.int32)
+    off = 0
+    for r, n in enumerate(npg):
+        pt[r, :n] = torch.arange(off, off + n, dtype=torch.int32)
+        off += n
+    q = (torch.randn(len(picks), spec.h_q, spec.d, generator=g) * spec.std).to(spec.dtype)
+
+    def step():
+        oracle.extend_attention(q, kc, vc, pt, list(range(len(picks) + 1)), [L - 1 for L in picks], spec.h_q,
+                                spec.h_kv)
+        return sum(4.0 * spec.d * spec.h_q * L for L in picks)
+    step.text = f"{len(picks)} decode rows x {spec.h_q} heads per step (all keys)"
+    return step
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cfg5", choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank, local)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

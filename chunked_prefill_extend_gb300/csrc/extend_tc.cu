@@ -1,0 +1,428 @@
+// Extend attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// One CTA computes one work unit: 128 query rows of one sequence that share a
+// KV head (kBlockM / G tokens x the G query heads of the group, so every K/V
+// tile staged in shared memory serves all G heads), against keys [0, kv_end).
+//
+// Key tiles of 128 are walked in order.  Tiles wholly inside the cached prefix
+// are the unmasked rectangle (Stage 1 of the SGLang chunked-prefill article);
+// tiles that reach the chunk's own keys form the causal triangle (Stage 2),
+// where only the tiles crossing the diagonal apply the mask j <= P + i and
+// tiles above it are never loaded.  Both stages feed one running (m, l, O)
+// per row: the article's online-softmax LSE merge of the two partials, applied
+// tile by tile.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q tile once, then K and V page boxes per key tile
+//               into an NS-stage ring (one box = 16 tokens x 64 dims, 128-byte
+//               swizzle; eight pages stack into one 128-key tile).
+//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
+//               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM.
+//   warps 2-5   softmax: one thread per query row reads its S row from TMEM,
+//               masks, updates the running max (rescaling O only when the max
+//               grows by more than 2^8), writes P as bf16 over its S columns,
+//               and finally normalises O and stores it.
+// TMEM columns: [0,128) S0, [128,256) S1, [256,256+D) O.
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// CPE_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
+// drained, TMEM is freed and the kernel returns.
+#include "cpe_device.cuh"
+#include "kernels.h"
+
+namespace cpe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint64_t kDrainNs = 2000000000ull;  // fixed bound for the final drain waits
+
+template <int D>
+struct TcCfg {
+  static constexpr int kHalves = D / 64;              // 128-byte column blocks per row
+  static constexpr int kTileBytes = kBlockM * D * 2;  // 128 rows (or keys) x D bf16
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kHalfBytes = 128 * 128;        // 128 rows x 128 bytes
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kSmem = kBarOff + 256 + 1024;  // + barriers + alignment slack
+};
+
+template <int NS>
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_full, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendTcArgs a) {
+  using C = TcCfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars<NS>* bars = reinterpret_cast<Bars<NS>*>(smem + C::kBarOff);
+
+  const TileEntry t = a.tiles[blockIdx.x];
+  if (t.seq < 0) return;  // unused slot of the tile list (uniform over the CTA)
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int s = t.seq;
+  const int g = t.kv_head;
+  const int q0 = a.qo_indptr[s];
+  const int E = a.qo_indptr[s + 1] - q0;
+  const int P = a.prefix_len[s];
+  const int i0 = t.q_tile * a.tok;
+  const int kv_end = P + min(E, i0 + a.tok);
+  const int n_kt = (kv_end + kBlockN - 1) / kBlockN;
+  volatile int* abort = &bars->abort;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+    }
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
+      for (int h = 0; h < C::kHalves; ++h)
+        tma_load_3d(smem + C::kQOff + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64,
+                    g * a.group, q0 + i0);
+      const int32_t* pt = a.page_table + static_cast<int64_t>(s) * a.max_pages;
+      const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int st = j % NS;
+        const int u = j / NS;
+        const int keys = min(kBlockN, kv_end - j * kBlockN);
+        const int npg = (keys + kPage - 1) / kPage;
+        int rows[kBlockN / kPage];
+        for (int pg = 0; pg < npg; ++pg) {
+          const int pid = pt[j * (kBlockN / kPage) + pg];
+          if (pid < 0 || pid >= a.num_pages) {
+            record_error(a.status, kStatusDeviceArg, kDetailBadPage);
+            rows[pg] = oob;
+          } else {
+            rows[pg] = pid * kPage;
+          }
+        }
+        const uint32_t bytes = npg * C::kHalves * (kPage * 128);
+        if (u > 0 && !mbar_wait(&bars->k_empty[st], (u - 1) & 1, abort, a.wait_ns, a.status, kDetailKEmpty))
+          break;
+        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+        for (int pg = 0; pg < npg; ++pg)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(smem + C::kKOff + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128),
+                        &a.tm_k, &bars->k_full[st], h * 64, g, rows[pg]);
+        if (u > 0 && !mbar_wait(&bars->v_empty[st], (u - 1) & 1, abort, a.wait_ns, a.status, kDetailVEmpty)) {
+          issued = -(j + 1);  // K of tile j issued, V not
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+        for (int pg = 0; pg < npg; ++pg)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(smem + C::kVOff + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128),
+                        &a.tm_v, &bars->v_full[st], h * 64, g, rows[pg]);
+        issued = j + 1;
+      }
+      // Drain: every copy issued must land before the CTA exits.
+      if (*abort) {
+        const int nk = issued >= 0 ? issued : -issued;
+        const int nv = issued >= 0 ? issued : -issued - 1;
+        volatile int no_abort = 0;
+        mbar_wait(&bars->q_full, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
+        for (int j = max(0, nk - NS); j < nk; ++j)
+          mbar_wait(&bars->k_full[j % NS], (j / NS) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+        for (int j = max(0, nv - NS); j < nv; ++j)
+          mbar_wait(&bars->v_full[j % NS], (j / NS) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+      const uint32_t sq = smem_u32(smem + C::kQOff);
+      bool ok = mbar_wait(&bars->q_full, 0, abort, a.wait_ns, a.status, kDetailQFull);
+      tc_fence_after();
+      for (int j = 0; ok && j <= n_kt; ++j) {
+        if (j < n_kt) {
+          const int b = j & 1;
+          const int st = j % NS;
+          if (j >= 2 && !mbar_wait(&bars->o_full, (j - 2) & 1, abort, a.wait_ns, a.status, kDetailOFull)) break;
+          if (!mbar_wait(&bars->k_full[st], (j / NS) & 1, abort, a.wait_ns, a.status, kDetailKFull)) break;
+          tc_fence_after();
+          const uint32_t sk = smem_u32(smem + C::kKOff + st * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+            tc_mma_ss(tmem + b * 128, smem_desc_sw128(sq + off, 16, 1024),
+                      smem_desc_sw128(sk + off, 16, 1024), idesc_qk, kk > 0);
+          }
+          tc_commit(&bars->k_empty[st]);
+          tc_commit(&bars->s_full[b]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          const int b = jj & 1;
+          const int st = jj % NS;
+          if (!mbar_wait(&bars->p_full[b], (jj / 2) & 1, abort, a.wait_ns, a.status, kDetailPFull)) break;
+          if (!mbar_wait(&bars->v_full[st], (jj / NS) & 1, abort, a.wait_ns, a.status, kDetailVFull)) break;
+          tc_fence_after();
+          const uint32_t sv = smem_u32(smem + C::kVOff + st * C::kTileBytes);
+          const int keys = min(kBlockN, kv_end - jj * kBlockN);
+          const int nsteps = (keys + 15) / 16;  // only pages that were loaded
+          for (int kk = 0; kk < nsteps; ++kk) {
+            tc_mma_ts(tmem + 256, tmem + b * 128 + kk * 8,
+                      smem_desc_sw128(sv + kk * (16 * 128), C::kHalfBytes, 1024), idesc_pv,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&bars->v_empty[st]);
+          tc_commit(&bars->o_full);
+        }
+      }
+      // Drain: wait until every MMA issued above has completed.
+      tc_commit(&bars->drain);
+      volatile int no_abort = 0;
+      mbar_wait(&bars->drain, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;             // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane;        // query row of the tile
+    const int i = i0 + r / a.group;        // token index within the chunk
+    const int lim = P + min(i, E - 1);     // last key this row may see
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&bars->s_full[b], (j / 2) & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
+      tc_fence_after();
+      float sv[kBlockN];
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld32(tmem + lane_base + b * 128 + c * 32, raw);
+        tc_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) sv[c * 32 + x] = __uint_as_float(raw[x]);
+      }
+      const int kb = j * kBlockN;
+      if (kb + kBlockN - 1 > P + i0) {  // tile crosses the diagonal or the end: mask
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c)
+          if (kb + c > lim) sv[c] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_tile = mx * sl2;
+      const bool grow = m_tile > m_run + 8.0f;
+      const float m_new = grow ? m_tile : m_run;
+      const float factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
+      m_run = m_new;
+      const float mbase = (m_run == -INFINITY) ? 0.f : m_run;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float p0 = fast_exp2(fmaf(sv[c * 32 + 2 * x], sl2, -mbase));
+          const float p1 = fast_exp2(fmaf(sv[c * 32 + 2 * x + 1], sl2, -mbase));
+          sum += p0 + p1;
+          pk[x] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tmem + lane_base + b * 128 + c * 16, pk);
+      }
+      l_run = l_run * factor + sum;
+      tc_wait_st();
+      if (j >= 1) {
+        // PV_{j-1} must be complete before O is rescaled or PV_j accumulates.
+        if (!mbar_wait(&bars->o_full, (j - 1) & 1, abort, a.wait_ns, a.status, kDetailOFull)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t raw[32];
+            tmem_ld32(tmem + lane_base + 256 + c * 32, raw);
+            tc_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * factor);
+            tmem_st32(tmem + lane_base + 256 + c * 32, raw);
+          }
+          tc_wait_st();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+    }
+    // epilogue: wait for the last PV, normalise, store
+    if (ok && n_kt > 0 &&
+        mbar_wait(&bars->o_full, (n_kt - 1) & 1, abort, a.wait_ns, a.status, kDetailOFull)) {
+      tc_fence_after();
+      const bool valid = i < E;
+      const float inv_l = 1.0f / l_run;
+      const int head = g * a.group + r % a.group;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                            (static_cast<int64_t>(q0 + i) * a.h_q + head) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld32(tmem + lane_base + 256 + c * 32, raw);
+        tc_wait_ld();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(raw[8 * x + 0]) * inv_l, __uint_as_float(raw[8 * x + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(raw[8 * x + 2]) * inv_l, __uint_as_float(raw[8 * x + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(raw[8 * x + 4]) * inv_l, __uint_as_float(raw[8 * x + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(raw[8 * x + 6]) * inv_l, __uint_as_float(raw[8 * x + 7]) * inv_l);
+            dst[x] = v;
+          }
+        }
+      }
+      if (valid && a.lse != nullptr)
+        a.lse[static_cast<int64_t>(q0 + i) * a.h_q + head] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Block-wide exclusive prefix sum (blockDim.x a multiple of 32, <= 1024).
+__device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int ws = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += y;
+    }
+    warp_sums[lane] = ws;
+  }
+  __syncthreads();
+  const int base = w > 0 ? warp_sums[w - 1] : 0;
+  *total = warp_sums[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__device__ int seq_tiles(const ScheduleArgs& a, int s, bool record) {
+  const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
+  const int P = a.prefix_len[s];
+  const bool bad = E < 0 || P < 0 || P + E > a.max_kv_len ||
+                   (P + E + kPage - 1) / kPage > a.max_pages;
+  if (bad && record) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
+  return bad ? 0 : (E + a.tok - 1) / a.tok;
+}
+
+// Tile list: for each KV head, each sequence's query tiles, last tile first
+// (the last tiles see the most keys).  Slots past the real count get seq = -1.
+__global__ void schedule_kernel(ScheduleArgs a) {
+  __shared__ int warp_sums[32];
+  const int n = a.seq_end - a.seq_begin;
+  int local = 0;
+  for (int k = threadIdx.x; k < n; k += blockDim.x) local += seq_tiles(a, a.seq_begin + k, true);
+  int total = 0;
+  block_exclusive_scan(local, &total, warp_sums);
+  int carry = 0;
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+    const int k = c0 + threadIdx.x;
+    const int s = a.seq_begin + k;
+    const int cnt = k < n ? seq_tiles(a, s, false) : 0;
+    int chunk_total = 0;
+    const int off = carry + block_exclusive_scan(cnt, &chunk_total, warp_sums);
+    for (int g = 0; g < a.h_kv; ++g)
+      for (int q = 0; q < cnt; ++q) {
+        const int idx = g * total + off + q;
+        if (idx < a.capacity) a.tiles[idx] = TileEntry{s, cnt - 1 - q, g, 0};
+      }
+    carry += chunk_total;
+  }
+  for (int idx = total * a.h_kv + threadIdx.x; idx < a.capacity; idx += blockDim.x)
+    a.tiles[idx] = TileEntry{-1, 0, 0, 0};
+}
+
+}  // namespace
+
+size_t extend_tc_smem_bytes(int d) {
+  return d == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem;
+}
+
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
+  schedule_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s) {
+  if (a.n_ctas <= 0) return cudaSuccess;
+  if (a.d == 128) {
+    const int smem = TcCfg<128>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    extend_tc_kernel<128><<<a.n_ctas, kThreads, smem, s>>>(a);
+  } else {
+    const int smem = TcCfg<64>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    extend_tc_kernel<64><<<a.n_ctas, kThreads, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace cpe

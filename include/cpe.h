@@ -1,0 +1,251 @@
+/*
+ * cpe.h — C ABI of libcpe, chunked-prefill extend attention on GB300 (sm_103a).
+ *
+ * The library computes one round of chunked prefill for a batch of sequences:
+ * sequence s has P_s tokens already in a paged KV cache (prefix_len) and E_s new
+ * query tokens at positions [P_s, P_s + E_s) (qo_indptr).  Each new query row i
+ * attends to keys [0, P_s + i]: the cached prefix as an unmasked rectangle and
+ * its own chunk as a causal triangle, merged by their log-sum-exp statistics.
+ *   SGLang chunked-prefill article (zdszero.github.io/chunked_prefill.html),
+ *   section "turning one prefill into resumable extends": P_t, E_t, S_t, the
+ *   output o_i, Stage 1 / Stage 2 and the online-softmax merge.
+ * Decode rows are sequences with E_s = 1 (context length L = P_s + 1).
+ *
+ * Conventions shared by every entry point
+ *  - The caller owns all memory.  The library allocates nothing and frees
+ *    nothing, and it never synchronises a stream except in
+ *    cpe_get_device_status().
+ *  - Host arrays are marked (host); every other pointer is device memory.
+ *  - Launches are asynchronous on the given stream (NULL = legacy default).
+ *  - Errors are returned as cpe_status, never thrown.  Argument errors are
+ *    found on the host before any launch and nothing is launched; a message is
+ *    available from cpe_last_error() on the calling thread.  Errors found on
+ *    the device (a page id out of range, a length above max_kv_len, a pipeline
+ *    wait that gave up) are recorded in a device status word that
+ *    cpe_get_device_status() reads and clears.
+ *  - Layouts are row-major with the last dimension contiguous:
+ *      q, out       [total_q, H_q, d]
+ *      k_new, v_new [total_q, H_kv, d]
+ *      k/v cache    [num_pages, page_size, H_kv, d]
+ *      page_table   [n_seqs, max_pages] int32 (page ids; entries past a
+ *                   sequence's last page are never read)
+ *      qo_indptr    [n_seqs + 1] int32, qo_indptr[0] = 0, non-decreasing,
+ *                   qo_indptr[n_seqs] = total_q
+ *      prefix_len   [n_seqs] int32
+ *      lse          [total_q, H_q] float32, natural log, m + ln(l) over the
+ *                   scaled scores
+ *  - Query head h reads KV head floor(h / G), G = H_q / H_kv.
+ *  - Supported: d in {64, 128}; H_q % H_kv == 0 and G in {1, 2, 4, 8, 16};
+ *    page_size = 16; dtype CPE_BF16 (bf16 in and out, fp32 accumulation) or
+ *    CPE_F32 (fp32 in and out).  Every device pointer 16-byte aligned.
+ */
+#ifndef CPE_H
+#define CPE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cpe_stream_t; /* the same type as cudaStream_t */
+
+typedef enum cpe_status {
+    CPE_OK = 0,
+    CPE_ERR_INVALID_ARG = 1, /* null pointer, length <= 0, inconsistent sizes     */
+    CPE_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set         */
+    CPE_ERR_CAPACITY = 3,    /* output or workspace buffer too small             */
+    CPE_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed             */
+    CPE_ERR_TIMEOUT = 5,     /* device: a pipeline wait gave up (kernel returned) */
+    CPE_ERR_DEVICE_ARG = 6   /* device: bad page id / length found in device data */
+} cpe_status;
+
+typedef enum cpe_dtype { CPE_F32 = 0, CPE_BF16 = 1 } cpe_dtype;
+
+/*
+ * One chunk of a chunked prefill.
+ *   msmodeling RFC "Chunked Prefill modelling support", section 3.1.3
+ *   (PrefillChunk: index, query_len, seq_len), extended with the cursor of the
+ *   SGLang article: the round computes positions [prefix_len, seq_len).
+ *   prefix_len    P_t: tokens before this chunk, cached prefix included
+ *   query_len     E_t: tokens computed in this chunk
+ *   seq_len       S_t = P_t + E_t
+ *   model_seq_len the RFC's seq_len: tokens of the effective (uncached) part
+ *                 consumed once this chunk is done (cached prefix left out)
+ */
+typedef struct cpe_chunk {
+    int32_t index;
+    int32_t prefix_len;
+    int32_t query_len;
+    int32_t seq_len;
+    int32_t model_seq_len;
+} cpe_chunk;
+
+/*
+ * cpe_plan_chunks — the chunk plan of one request (host only).
+ *   msmodeling RFC, section 2.2: cached = floor(input_len * prefix_hit_rate)
+ *   in IEEE double, effective = input_len - cached; section 3.1.3: chunks of
+ *   min(chunk_size, remaining) tokens.  SGLang article, implementation
+ *   section: with align_to > 0 only a truncated first chunk has its absolute
+ *   end rounded down to a multiple of align_to (0 = no alignment).
+ * out (host) receives up to cap records; *n_out (host) the number of chunks.
+ * cached_out / effective_out (host, nullable) receive the two lengths; the
+ * decode context stays input_len.
+ * Errors: CPE_ERR_INVALID_ARG if chunk_size <= 0, input_len <= 0, the hit
+ * rate is outside [0, 1], effective < 1, align_to < 0, or a position exceeds
+ * INT32_MAX; CPE_ERR_CAPACITY if cap is below the chunk count (*n_out still
+ * holds the count).
+ */
+cpe_status cpe_plan_chunks(int64_t input_len, double prefix_hit_rate, int32_t chunk_size,
+                           int32_t align_to, cpe_chunk* out, int32_t cap, int32_t* n_out,
+                           int64_t* cached_out, int64_t* effective_out);
+
+/*
+ * cpe_plan_budget — token-budget truncation (host only).
+ *   vLLM token-budget tutorial, section 5: requests in order each take
+ *   min(need, remaining budget); a decode request needs 1 token.
+ * need[n_req] (host) in, granted[n_req] (host) out, *used (host, nullable) =
+ * sum of granted.  Errors: CPE_ERR_INVALID_ARG for token_budget <= 0,
+ * n_req < 0, a negative need, or null arrays with n_req > 0.
+ */
+cpe_status cpe_plan_budget(int32_t token_budget, int32_t n_req, const int32_t* need,
+                           int32_t* granted, int32_t* used);
+
+/*
+ * cpe_plan_mixed_step — one mixed step: decode rows first, then one prefill
+ * chunk from the budget that is left (host only).
+ *   vLLM tutorial, section 5 (running requests first, one token per decode);
+ *   SGLang article, mixed-chunk section (the chunk shrinks by the number of
+ *   running decode requests).
+ * decode_ctx_len[n_decode] (host): each decode row's context length L >= 1,
+ * the token appended this step included (its cached prefix is L-1).
+ * The prefill request has prefill_prefix_len tokens cached and
+ * prefill_remaining still to compute.
+ * Outputs (host), for the scheduled sequences in batch order (decode rows
+ * first; rows that did not fit are left out, in order; the prefill sequence
+ * last if it got any tokens):
+ *   qo_indptr[n_decode + 2], prefix_len[n_decode + 1], kv_len[n_decode + 1],
+ *   *n_seqs, *n_decode_out (decode rows scheduled), *extend_len_out.
+ * Errors: CPE_ERR_INVALID_ARG for token_budget <= 0, n_decode < 0, L < 1,
+ * negative prefill lengths, or null outputs.
+ */
+cpe_status cpe_plan_mixed_step(int32_t token_budget, int32_t n_decode,
+                               const int32_t* decode_ctx_len, int32_t prefill_prefix_len,
+                               int32_t prefill_remaining, int32_t* qo_indptr, int32_t* prefix_len,
+                               int32_t* kv_len, int32_t* n_seqs, int32_t* n_decode_out,
+                               int32_t* extend_len_out);
+
+/*
+ * cpe_kv_append — write the round's new K/V rows into the paged caches.
+ *   SGLang article, implementation section (the request's req_to_token row
+ *   keeps its page slots across chunks); mini-infer article, write_prefill_kv.
+ * Row r of sequence s (qo_indptr[s] <= r < qo_indptr[s+1]) goes to position
+ * pos = prefix_len[s] + r - qo_indptr[s], i.e. page page_table[s][pos /
+ * page_size], slot pos % page_size.  A bitwise copy.
+ * Device errors: a page id outside [0, num_pages) or pos / page_size >=
+ * max_pages skips the row and records CPE_ERR_DEVICE_ARG.
+ */
+cpe_status cpe_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                         const int32_t* qo_indptr, const int32_t* prefix_len, int32_t n_seqs,
+                         int32_t total_q, int32_t h_kv, int32_t d, int32_t page_size,
+                         cpe_dtype dtype, cpe_stream_t stream);
+
+/*
+ * cpe_workspace_size — bytes of device workspace the attention entry points
+ * need for these sizes (the tile list and split-KV partial results).
+ * max_kv_len bounds prefix_len[s] + E_s over all sequences.
+ */
+size_t cpe_workspace_size(int32_t n_seqs, int32_t total_q, int32_t h_q, int32_t h_kv, int32_t d,
+                          int32_t max_kv_len);
+
+/*
+ * cpe_extend_attention — the extend output for every query row (all rows of
+ * all sequences): out[r, h] = sum_{j <= P_s + i} softmax_j(q . k_j * sm_scale) v_j.
+ *   SGLang article, equation for o_i; Stage 1 (prefix rectangle, no mask) and
+ *   Stage 2 (causal triangle in the chunk) run as separate tile classes whose
+ *   partials are merged by their (m, l) statistics.
+ * The keys of the chunk itself (positions [P_s, P_s + E_s)) must already be
+ * in the cache (cpe_kv_append first).
+ * sm_scale: softmax scale (pass 1/sqrt(d) for the pages' definition).
+ * max_kv_len: an upper bound on prefix_len[s] + E_s; sequences above it are
+ * not computed and CPE_ERR_DEVICE_ARG is recorded.
+ * lse: nullable.  workspace: at least cpe_workspace_size(...) bytes, 256-byte
+ * aligned; its contents need not be initialised and are clobbered.
+ * Errors: CPE_ERR_INVALID_ARG / CPE_ERR_UNSUPPORTED / CPE_ERR_CAPACITY before
+ * any launch; CPE_ERR_CUDA if a launch fails.
+ */
+cpe_status cpe_extend_attention(const void* q, const void* k_cache, const void* v_cache,
+                                int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                                const int32_t* qo_indptr, const int32_t* prefix_len,
+                                int32_t n_seqs, int32_t total_q, int32_t max_kv_len, int32_t h_q,
+                                int32_t h_kv, int32_t d, int32_t page_size, float sm_scale,
+                                cpe_dtype dtype, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cpe_stream_t stream);
+
+/*
+ * cpe_mixed_step — one mixed forward step of attention: n_decode decode rows
+ * (sequences 0 .. n_decode-1, one query each) and the remaining sequences'
+ * prefill chunks, under one token budget, as cpe_plan_mixed_step lays them out.
+ *   SGLang article, mixed-chunk section (ForwardMode.MIXED); vLLM tutorial,
+ *   section 4 ({request_id: num_tokens} in one forward).
+ * Appends k_new / v_new for every row (as cpe_kv_append), then computes the
+ * decode rows with the split-KV path (HBM-bound, one CTA per (row, KV head,
+ * split), merged by LSE) and the prefill chunks with the extend path.
+ * Same arguments as cpe_extend_attention plus k_new, v_new, the writable
+ * caches and n_decode (0 <= n_decode <= n_seqs).  A decode sequence whose
+ * query length is not 1 records CPE_ERR_DEVICE_ARG and is not computed.
+ */
+cpe_status cpe_mixed_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                          void* v_cache, int64_t num_pages, const int32_t* page_table,
+                          int32_t max_pages, const int32_t* qo_indptr, const int32_t* prefix_len,
+                          int32_t n_seqs, int32_t n_decode, int32_t total_q, int32_t max_kv_len,
+                          int32_t h_q, int32_t h_kv, int32_t d, int32_t page_size, float sm_scale,
+                          cpe_dtype dtype, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, cpe_stream_t stream);
+
+/*
+ * cpe_decode_attention — the decode-row path on its own: every sequence has
+ * one query row (qo_indptr[s] = s).  Split-KV over each row's context, merged
+ * by LSE.  Arguments as cpe_extend_attention.
+ */
+cpe_status cpe_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                                const int32_t* prefix_len, int32_t n_seqs, int32_t max_kv_len,
+                                int32_t h_q, int32_t h_kv, int32_t d, int32_t page_size,
+                                float sm_scale, cpe_dtype dtype, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, cpe_stream_t stream);
+
+/*
+ * cpe_get_device_status — synchronise `stream`, then read and clear the
+ * device status word of the current device.  Returns CPE_OK, the first device
+ * error recorded since the last call (CPE_ERR_TIMEOUT, CPE_ERR_DEVICE_ARG), or
+ * CPE_ERR_CUDA if the synchronisation itself failed.  *detail (host,
+ * nullable) receives a code naming the wait or check that failed.
+ */
+cpe_status cpe_get_device_status(cpe_stream_t stream, int32_t* detail);
+
+/*
+ * cpe_set_wait_limit_ns — time after which a device pipeline wait gives up,
+ * records CPE_ERR_TIMEOUT and lets its kernel return (default 4e9 ns).  A
+ * test hook: 0 makes every wait that is not already satisfied give up at
+ * once, so the timeout path can be checked without a stalled kernel.
+ * Applies to launches made after the call; returns the previous value.
+ */
+int64_t cpe_set_wait_limit_ns(int64_t ns);
+
+/* Static description of a status code. */
+const char* cpe_status_string(cpe_status status);
+
+/* Message of the last host-side error on the calling thread ("" if none). */
+const char* cpe_last_error(void);
+
+/* Number of CUDA kernels this library has launched in this process. */
+int64_t cpe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPE_H */

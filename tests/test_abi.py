@@ -1,0 +1,114 @@
+"""The C-ABI library loads, exports what include/cpe.h declares, validates
+arguments on the host, and its planners match the oracle's bit for bit.
+No CUDA call is made here (host-only entry points and pre-launch checks)."""
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+from chunked_prefill_extend_gb300 import cpe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "cpe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert "cpe_extend_attention" in names and "cpe_mixed_step" in names and "cpe_kv_append" in names
+    for n in names:
+        assert hasattr(cpe._lib, n), f"libcpe.so does not export {n}"
+    assert sorted(cpe.EXPORTS) == names
+
+
+@pytest.mark.parametrize("n,hit,c,align", [(4000, 0.0, 512, 0), (32768, 0.5, 8192, 0), (131072, 0.0, 1024, 0),
+                                           (10000, 0.0, 4096, 0), (4096, 0.0, 8192, 0), (1000, 0.01, 100, 16),
+                                           (1, 0.0, 1, 0), (99991, 0.37, 333, 16), (7, 0.5, 2, 4)])
+def test_plan_chunks_matches_oracle(n, hit, c, align):
+    chunks, cached, eff = cpe.cpe_plan_chunks(n, hit, c, align)
+    ref = oracle.plan_chunks(n, hit, c, align)
+    assert [tuple(vars(x).values()) for x in chunks] == [tuple(vars(x).values()) for x in ref]
+    assert (cached, eff) == oracle.effective_input_length(n, hit)
+
+
+def test_plan_chunks_random_against_oracle():
+    rng = random.Random(7)
+    for _ in range(300):
+        n = rng.randint(1, 200000)
+        hit = rng.choice([0.0, 0.5, rng.random()])
+        c = rng.randint(1, 9000)
+        align = rng.choice([0, 0, 16, 64])
+        try:
+            ref = oracle.plan_chunks(n, hit, c, align)
+        except ValueError:
+            with pytest.raises(cpe.CpeError):
+                cpe.cpe_plan_chunks(n, hit, c, align)
+            continue
+        got, _, _ = cpe.cpe_plan_chunks(n, hit, c, align)
+        assert [tuple(vars(x).values()) for x in got] == [tuple(vars(x).values()) for x in ref]
+
+
+@pytest.mark.parametrize("bad", [0, -1])
+def test_plan_chunks_rejects_nonpositive_chunk(bad):
+    with pytest.raises(cpe.CpeError) as e:
+        cpe.cpe_plan_chunks(1000, 0.0, bad)
+    assert e.value.status == cpe.CPE_ERR_INVALID_ARG
+
+
+def test_plan_budget_and_mixed_step_match_oracle():
+    rng = random.Random(11)
+    for _ in range(200):
+        budget = rng.randint(1, 5000)
+        needs = [rng.randint(0, 3000) for _ in range(rng.randint(0, 12))]
+        got, used = cpe.cpe_plan_budget(budget, needs)
+        assert got == oracle.budget_truncate(budget, needs) and used == sum(got)
+        ctx = [rng.randint(1, 40000) for _ in range(rng.randint(0, 300))]
+        P, rem = rng.randint(0, 50000), rng.randint(0, 9000)
+        a = cpe.cpe_plan_mixed_step(budget, ctx, P, rem)
+        b = oracle.plan_mixed_step(budget, ctx, P, rem)
+        assert a == b
+
+
+def test_mixed_step_cfg4_shape():
+    out = cpe.cpe_plan_mixed_step(2304, [1000] * 256, 30720, 4096)
+    assert out["extend_len"] == 2048 and out["n_decode"] == 256 and out["qo_indptr"][-1] == 2304
+
+
+def test_host_validation_happens_before_any_launch():
+    """Bad arguments come back as status codes; nothing touches a device."""
+    f = cpe._lib.cpe_extend_attention
+    fake = 1 << 20  # never dereferenced: validation fails first
+    args = dict(q=fake, k=fake, v=fake, num_pages=10, pt=fake, max_pages=4, qo=fake, pl=fake, n_seqs=1,
+                total_q=16, max_kv=64, h_q=32, h_kv=8, d=128, page=16, scale=0.088, dt=cpe.CPE_BF16,
+                out=fake, lse=None, ws=fake, ws_bytes=1 << 30, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["q"], a["k"], a["v"], a["num_pages"], a["pt"], a["max_pages"], a["qo"], a["pl"], a["n_seqs"],
+                 a["total_q"], a["max_kv"], a["h_q"], a["h_kv"], a["d"], a["page"], a["scale"], a["dt"], a["out"],
+                 a["lse"], a["ws"], a["ws_bytes"], a["stream"])
+
+    assert call(q=None) == cpe.CPE_ERR_INVALID_ARG
+    assert call(d=96) == cpe.CPE_ERR_UNSUPPORTED
+    assert call(page=32) == cpe.CPE_ERR_UNSUPPORTED
+    assert call(h_q=24, h_kv=8) == cpe.CPE_ERR_UNSUPPORTED       # G = 3
+    assert call(h_q=30, h_kv=8) == cpe.CPE_ERR_INVALID_ARG       # not a multiple
+    assert call(n_seqs=0) == cpe.CPE_ERR_INVALID_ARG
+    assert call(ws_bytes=16) == cpe.CPE_ERR_CAPACITY
+    assert call(q=fake + 8) == cpe.CPE_ERR_INVALID_ARG           # misaligned
+    assert call(scale=float("nan")) == cpe.CPE_ERR_INVALID_ARG
+    assert "workspace" in cpe.cpe_last_error() or "scale" in cpe.cpe_last_error()
+    assert cpe.cpe_status_string(cpe.CPE_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_workspace_size_is_monotone_and_zero_for_bad_sizes():
+    a = cpe.cpe_workspace_size(1, 512, 32, 8, 128, 4000)
+    b = cpe.cpe_workspace_size(257, 2304, 32, 8, 128, 32768)
+    assert 0 < a < b and b % 256 == 0
+    assert cpe.cpe_workspace_size(0, 1, 32, 8, 128, 10) == 0

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small cases are compared element by element; the full-size workloads on
+sampled rows (first, last, both sides of tile boundaries, seeded picks).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_prefill_extend_gb300 import workloads as W
+from tests._util import check_close, extract_pages, i32, varlen_batch, LSE_ABS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cpe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunked_prefill_extend_gb300 import cpe as lib
+    st, _ = lib.cpe_get_device_status()
+    assert st == lib.CPE_OK
+    return lib
+
+
+def _status_ok(cpe):
+    st, detail = cpe.cpe_get_device_status()
+    assert st == cpe.CPE_OK, f"device status {cpe.cpe_status_string(st)} detail {detail}"
+
+
+def _append_and_attend(cpe, b, lse=True):
+    qo, pl = i32(b["qo"]), i32(b["pl"])
+    cpe.cpe_kv_append(b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"], qo, pl)
+    lse_t = torch.empty(b["q"].shape[0], b["h_q"], dtype=torch.float32, device="cuda") if lse else None
+    out, _ = cpe.cpe_extend_attention(b["q"], b["k_cache"], b["v_cache"], b["page_table"], qo, pl, b["max_kv"],
+                                      lse=lse_t)
+    _status_ok(cpe)
+    return out, lse_t
+
+
+def _oracle_batch(b):
+    return oracle.extend_attention(b["q"].cpu(), b["k_cache"].cpu(), b["v_cache"].cpu(), b["page_table_host"],
+                                   b["qo"], b["pl"], b["h_q"], b["h_kv"])
+
+
+# ---------------------------------------------------------------- kv append
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_kv_append_bitwise(cpe, dtype):
+    b = varlen_batch(1, [(0, 40), (17, 1), (100, 77), (5, 0), (33, 16)], 8, 2, 128, dtype=dtype)
+    kc_ref, vc_ref = b["k_cache"].cpu().clone(), b["v_cache"].cpu().clone()
+    oracle.kv_append(b["k_new"].cpu(), b["v_new"].cpu(), kc_ref, vc_ref, b["page_table_host"], b["qo"], b["pl"])
+    cpe.cpe_kv_append(b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"], i32(b["qo"]),
+                      i32(b["pl"]))
+    _status_ok(cpe)
+    assert torch.equal(b["k_cache"].cpu(), kc_ref) and torch.equal(b["v_cache"].cpu(), vc_ref)
+
+
+# ---------------------------------------------------------------- extend, small, full compare
+
+SMALL = [
+    # (seed, [(P, E), ...], h_q, h_kv, d)
+    (10, [(0, 1)], 32, 8, 128),                       # one key
+    (11, [(0, 300)], 32, 8, 128),                     # P = 0, several tiles, ragged tail
+    (12, [(517, 45)], 32, 8, 128),                    # prefix + short chunk
+    (13, [(129, 1)], 32, 8, 128),                     # E = 1 at a tile boundary
+    (14, [(100, 64), (0, 33), (2000, 130), (7, 0), (256, 128)], 32, 8, 128),  # varlen incl. empty
+    (15, [(300, 200)], 8, 8, 128),                    # G = 1
+    (16, [(250, 170)], 16, 8, 128),                   # G = 2
+    (17, [(333, 99)], 64, 8, 128),                    # G = 8
+    (18, [(140, 77)], 32, 2, 128),                    # G = 16
+    (19, [(411, 150), (0, 20)], 32, 8, 64),           # d = 64
+    (20, [(1000, 257)], 8, 1, 64),                    # G = 8, d = 64
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"seed{c[0]}")
+def test_extend_small_full(cpe, case):
+    seed, lens, h_q, h_kv, d = case
+    b = varlen_batch(seed, lens, h_q, h_kv, d)
+    out, lse = _append_and_attend(cpe, b)
+    ref_o, ref_l = _oracle_batch(b)
+    check_close(out, ref_o, f"out {case}")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
+def test_extend_fp32_path(cpe):
+    b = varlen_batch(21, [(50, 70), (0, 9)], 4, 4, 64, dtype=torch.float32, std=1.0)
+    out, lse = _append_and_attend(cpe, b)
+    ref_o, ref_l = _oracle_batch(b)
+    check_close(out, ref_o, "fp32", max_abs=1e-4, rel_rms=1e-5)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=1e-4, rtol=0)
+
+
+def test_page_permutation_gives_bitwise_equal_output(cpe):
+    b = varlen_batch(22, [(700, 300)], 32, 8, 128)
+    out_a, _ = _append_and_attend(cpe, b, lse=False)
+    perm = torch.randperm(b["k_cache"].shape[0], generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(len(perm))
+    b2 = dict(b)
+    b2["k_cache"] = b["k_cache"][perm.cuda()].contiguous()
+    b2["v_cache"] = b["v_cache"][perm.cuda()].contiguous()
+    pth = b["page_table_host"]
+    b2["page_table_host"] = torch.where(pth >= 0, inv[pth.clamp(min=0).long()].to(torch.int32), pth)
+    b2["page_table"] = b2["page_table_host"].cuda()
+    out_b, _ = _append_and_attend(cpe, b2, lse=False)
+    assert torch.equal(out_a, out_b)
+
+
+# ---------------------------------------------------------------- chunked == one-shot
+
+def _chunked_run(cpe, spec, device="cuda"):
+    req = W.make_chunked(spec, device=device)
+    chunks, _, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+    outs = []
+    for ch in chunks:
+        q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
+        qo, pl = i32([0, ch.query_len]), i32([ch.prefix_len])
+        cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, qo, pl)
+        out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, qo, pl, ch.seq_len)
+        outs.append(out)
+    _status_ok(cpe)
+    return req, chunks, torch.cat(outs)
+
+
+def test_cfg1_chunked_equals_one_shot_fp32(cpe):
+    spec = W.CONFIGS["cfg1"]
+    req, chunks, out = _chunked_run(cpe, spec)
+    assert [c.query_len for c in chunks] == [128] * 4
+    one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
+    check_close(out, one, "cfg1 chunked vs one-shot", max_abs=1e-4, rel_rms=1e-5)
+    # the GPU's own one-shot run (one chunk of 512) agrees with its chunked run
+    spec1 = W.shrink(spec, chunk=512)
+    _, _, out1 = _chunked_run(cpe, spec1)
+    check_close(out, out1.double().cpu().numpy(), "cfg1 gpu chunked vs gpu one-shot", max_abs=1e-4, rel_rms=1e-5)
+
+
+def test_bf16_chunked_equals_one_shot(cpe):
+    spec = W.shrink(W.CONFIGS["cfg2"], input_len=1500, chunk=256)
+    req, _, out = _chunked_run(cpe, spec)
+    one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
+    check_close(out, one, "bf16 chunked vs one-shot")
+    _, _, out1 = _chunked_run(cpe, W.shrink(spec, chunk=1500))
+    check_close(out, out1.double().cpu().numpy(), "bf16 gpu chunked vs gpu one-shot")
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def test_cfg2_full(cpe):
+    spec = W.CONFIGS["cfg2"]
+    req, chunks, out = _chunked_run(cpe, spec)
+    assert [c.query_len for c in chunks] == [512] * 7 + [416]
+    one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
+    check_close(out, one, "cfg2 all rows")
+
+
+def _sampled_rounds(cpe, spec, round_ids, n_rows, seed):
+    req = W.make_chunked(spec, device="cuda")
+    chunks, cached, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+    for ch in chunks:  # every round's keys go into the cache first
+        q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
+        cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, i32([0, ch.query_len]),
+                          i32([ch.prefix_len]))
+    kc, vc = req.k_cache.cpu(), req.v_cache.cpu()
+    G = spec.h_q // spec.h_kv
+    for t in round_ids:
+        ch = chunks[t]
+        q, _, _ = req.round_inputs(ch.prefix_len, ch.query_len)
+        lse = torch.empty(ch.query_len, spec.h_q, dtype=torch.float32, device="cuda")
+        out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, i32([0, ch.query_len]),
+                                          i32([ch.prefix_len]), ch.seq_len, lse=lse)
+        _status_ok(cpe)
+        rows = W.sample_rows(ch.query_len, 128 // G, n_rows, seed + t)
+        ref_o, ref_l = oracle.extend_attention(q.cpu(), kc, vc,
+                                               torch.tensor([req.page_table_host], dtype=torch.int32),
+                                               [0, ch.query_len], [ch.prefix_len], spec.h_q, spec.h_kv, rows=rows)
+        check_close(out[rows], ref_o, f"{spec.name} round {t}")
+        np.testing.assert_allclose(lse[rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+    return chunks
+
+
+def test_cfg3_sampled(cpe):
+    chunks = _sampled_rounds(cpe, W.CONFIGS["cfg3"], [0, 1], 96, 300)
+    assert [(c.prefix_len, c.query_len) for c in chunks] == [(16384, 8192), (24576, 8192)]
+
+
+def test_cfg5_sampled(cpe):
+    chunks = _sampled_rounds(cpe, W.CONFIGS["cfg5"], [0, 7, 127], 24, 500)
+    assert len(chunks) == 128 and chunks[-1].seq_len == 131072
+
+
+# ---------------------------------------------------------------- decode rows
+
+@pytest.mark.parametrize("lens", [[1, 2, 15, 16, 17, 100], [2047, 2048, 2049, 4096, 4097, 9000], [32768, 1, 513]])
+def test_decode_rows(cpe, lens):
+    """Decode rows (E = 1 at P = L-1) through the split-KV path."""
+    b = varlen_batch(40 + len(lens), [(L - 1, 1) for L in lens], 32, 8, 128)
+    qo, pl = i32(b["qo"]), i32(b["pl"])
+    cpe.cpe_kv_append(b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"], qo, pl)
+    lse = torch.empty(len(lens), 32, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_decode_attention(b["q"], b["k_cache"], b["v_cache"], b["page_table"], pl, b["max_kv"], lse=lse)
+    _status_ok(cpe)
+    ref_o, ref_l = _oracle_batch(b)
+    check_close(out, ref_o, f"decode {lens}")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
+def test_mixed_step_small_full(cpe):
+    ctx = [1, 37, 2048, 2049, 5000, 300, 16, 999]
+    plan = cpe.cpe_plan_mixed_step(8 + 200, ctx, 3000, 500)
+    assert plan["n_decode"] == 8 and plan["extend_len"] == 200
+    lens = [(p, plan["qo_indptr"][i + 1] - plan["qo_indptr"][i]) for i, p in enumerate(plan["prefix_len"])]
+    b = varlen_batch(50, lens, 32, 8, 128)
+    lse = torch.empty(b["q"].shape[0], 32, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(b["q"], b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"],
+                                i32(b["qo"]), i32(b["pl"]), plan["n_decode"], b["max_kv"], lse=lse)
+    _status_ok(cpe)
+    kc, vc = b["k_cache"].cpu().clone(), b["v_cache"].cpu().clone()
+    ref_o, ref_l = oracle.extend_attention(b["q"].cpu(), kc, vc, b["page_table_host"], b["qo"], b["pl"], 32, 8)
+    check_close(out, ref_o, "mixed small")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
+def test_cfg4_mixed_sampled(cpe):
+    spec = W.CONFIGS["cfg4"]
+    g = torch.Generator().manual_seed(spec.seed)
+    ctx = torch.randint(spec.ctx_lo, spec.ctx_hi + 1, (spec.n_decode,), generator=g).tolist()
+    plan = cpe.cpe_plan_mixed_step(spec.token_budget, ctx, spec.prefill_prefix, spec.prefill_remaining)
+    assert plan["extend_len"] == 2048 and plan["n_decode"] == 256
+    mb = W.make_mixed(spec, plan["extend_len"], device="cuda")
+    plan = cpe.cpe_plan_mixed_step(spec.token_budget, mb.ctx_len, spec.prefill_prefix, spec.prefill_remaining)
+    max_kv = max(plan["kv_len"])
+    lse = torch.empty(mb.q.shape[0], spec.h_q, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(mb.q, mb.k_new, mb.v_new, mb.k_cache, mb.v_cache, mb.page_table,
+                                i32(plan["qo_indptr"]), i32(plan["prefix_len"]), plan["n_decode"], max_kv, lse=lse)
+    _status_ok(cpe)
+    # decode rows: the longest, the shortest and a seeded sample
+    order = sorted(range(256), key=lambda s: mb.ctx_len[s])
+    dec = sorted(set([order[0], order[-1]] + torch.randperm(256, generator=g)[:10].tolist()))
+    kl = [plan["kv_len"][s] for s in dec]
+    kc, vc, pt = extract_pages(mb.k_cache, mb.v_cache, mb.page_table_host, dec, kl)
+    q = mb.q[dec].cpu()
+    ref_o, ref_l = oracle.extend_attention(q, kc, vc, pt, list(range(len(dec) + 1)),
+                                           [plan["prefix_len"][s] for s in dec], spec.h_q, spec.h_kv)
+    check_close(out[dec], ref_o, "cfg4 decode rows")
+    np.testing.assert_allclose(lse[dec].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+    # prefill rows
+    ps = 256
+    kc, vc, pt = extract_pages(mb.k_cache, mb.v_cache, mb.page_table_host, [ps], [plan["kv_len"][ps]])
+    rows = W.sample_rows(2048, 32, 64, 404)
+    q = mb.q[256:]
+    ref_o, ref_l = oracle.extend_attention(q.cpu(), kc, vc, pt, [0, 2048], [plan["prefix_len"][ps]], spec.h_q,
+                                           spec.h_kv, rows=rows)
+    check_close(out[256:][rows], ref_o, "cfg4 prefill rows")
+    np.testing.assert_allclose(lse[256:][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
+# ---------------------------------------------------------------- device-side errors
+
+def test_bad_page_id_is_reported(cpe):
+    b = varlen_batch(60, [(40, 30)], 32, 8, 128)
+    b["page_table"][0, 1] = 10 ** 6  # out of range
+    qo, pl = i32(b["qo"]), i32(b["pl"])
+    cpe.cpe_extend_attention(b["q"], b["k_cache"], b["v_cache"], b["page_table"], qo, pl, b["max_kv"])
+    st, _ = cpe.cpe_get_device_status()
+    assert st == cpe.CPE_ERR_DEVICE_ARG
+    _status_ok(cpe)  # cleared by the read
+
+
+def test_wait_timeout_path_returns_status(cpe):
+    """With a zero wait limit every pipeline wait that is not already
+    satisfied gives up: the kernel records a timeout and returns, and the
+    context stays usable."""
+    b = varlen_batch(61, [(1000, 300)], 32, 8, 128)
+    qo, pl = i32(b["qo"]), i32(b["pl"])
+    old = cpe.cpe_set_wait_limit_ns(0)
+    try:
+        cpe.cpe_extend_attention(b["q"], b["k_cache"], b["v_cache"], b["page_table"], qo, pl, b["max_kv"])
+        st, _ = cpe.cpe_get_device_status()
+    finally:
+        cpe.cpe_set_wait_limit_ns(old)
+    assert st == cpe.CPE_ERR_TIMEOUT
+    out, _ = _append_and_attend(cpe, b)
+    ref_o, _ = _oracle_batch(b)
+    check_close(out, ref_o, "after timeout")
