@@ -28,7 +28,7 @@ CPE_F32, CPE_BF16 = 0, 1
 EXPORTS = ["cpe_plan_chunks", "cpe_plan_budget", "cpe_plan_mixed_step", "cpe_kv_append",
            "cpe_workspace_size", "cpe_extend_attention", "cpe_mixed_step", "cpe_decode_attention",
            "cpe_get_device_status", "cpe_set_wait_limit_ns", "cpe_status_string", "cpe_last_error",
-           "cpe_launch_count"]
+           "cpe_launch_count", "cpe_decode_attention_noalloc"]
 
 _vp, _i32, _i64, _f32, _f64, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                     ctypes.c_double, ctypes.c_size_t)
@@ -54,6 +54,8 @@ _lib.cpe_mixed_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _
                                 _i32, _i32, _i32, _i32, _f32, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]
 _lib.cpe_decode_attention.argtypes = [_vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                       _i32, _f32, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]
+_lib.cpe_decode_attention_noalloc.argtypes = [_vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                              _i32, _i32, _f32, ctypes.c_int, _vp, _vp, _vp]
 _lib.cpe_get_device_status.argtypes = [_vp, ctypes.POINTER(_i32)]
 _lib.cpe_set_wait_limit_ns.argtypes = [_i64]
 _lib.cpe_set_wait_limit_ns.restype = _i64
@@ -213,6 +215,25 @@ def cpe_mixed_step(q, k_new, v_new, k_cache, v_cache, page_table, qo_indptr, pre
                                n_decode, total_q, max_kv_len, h_q, h_kv, d, page_size, sm_scale, _dtype(q),
                                _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
            "cpe_mixed_step")
+    return out, lse
+
+
+def cpe_decode_attention_noalloc(q, k_cache, v_cache, page_table, prefix_len, max_kv_len, out=None, lse=None,
+                                 sm_scale=None, stream=None):
+    """cpe_decode_attention without a workspace: for callers that cannot allocate
+    device memory, the split partials live in the library's fixed 8 MiB device
+    array (see include/cpe.h for its limits).  ``out`` must be given by such a
+    caller; passing None lets torch allocate it here, for convenience only."""
+    n_seqs, h_q, d = q.shape
+    num_pages, page_size, h_kv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    _check(_lib.cpe_decode_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(page_table),
+                                             page_table.shape[1], _ptr(prefix_len), n_seqs, max_kv_len, h_q, h_kv,
+                                             d, page_size, sm_scale, _dtype(q), _ptr(out), _ptr(lse),
+                                             _stream(stream)), "cpe_decode_attention_noalloc")
     return out, lse
 
 

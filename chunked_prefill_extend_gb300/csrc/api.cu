@@ -226,6 +226,10 @@ cpe_status run_decode(const char* fn, const Common& c, int n_dec, bool use_qo, i
 
 void set_last_error(const std::string& msg) { t_last_error = msg; }
 
+int* device_status_word(cudaError_t* err) { return status_ptr(err); }
+
+void count_launches(int n) { g_launches += n; }
+
 }  // namespace cpe
 
 using namespace cpe;

@@ -218,6 +218,47 @@ cpe_status cpe_decode_attention(const void* q, const void* k_cache, const void* 
                                 void* workspace, size_t workspace_bytes, cpe_stream_t stream);
 
 /*
+ * cpe_decode_attention_noalloc — the decode-row path of cpe_decode_attention
+ * for callers that cannot allocate device memory.  The pages describe no such
+ * entry point; it has no counterpart there.
+ *
+ * Who needs it: a caller that may not call cudaMalloc or any allocator of its
+ * own — for instance a plugin inside a host program that owns every byte of
+ * device memory through its own pool, or a serving loop that must not enter
+ * an allocator on its hot path (cudaMalloc can synchronise the device and can
+ * fail when memory is fragmented).  cpe_decode_attention needs a caller-made
+ * workspace for its split partials; this entry point keeps them instead in a
+ * fixed array of CPE_DECODE_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory
+ * that the library declares statically, so the call itself allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * Arguments, layouts and results are those of cpe_decode_attention, without
+ * the workspace.  Limits and behaviour:
+ *  - The scratch needed is n_seqs * h_q * ceil(max_kv_len / 2048) * (d + 2)
+ *    * 4 bytes (each part rounded up to 256 bytes).  Above 8 MiB the call
+ *    returns CPE_ERR_CAPACITY before any launch; split the batch or use
+ *    cpe_decode_attention.  Only bf16 is taken (CPE_ERR_UNSUPPORTED).
+ *  - The array exists on every GPU that loads the library and stays there
+ *    until the process exits.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *    first call before any stream capture.
+ *  - Every call uses the same array, which keeps the last call's contents.
+ *    Nothing in it has to start at zero: each call writes every partial it
+ *    reads.  Calls whose kernels overlap on the GPU (different streams, or
+ *    different host threads, on one device) race on the array: order them on
+ *    one stream or synchronise between them.
+ */
+cpe_status cpe_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        int64_t num_pages, const int32_t* page_table,
+                                        int32_t max_pages, const int32_t* prefix_len, int32_t n_seqs,
+                                        int32_t max_kv_len, int32_t h_q, int32_t h_kv, int32_t d,
+                                        int32_t page_size, float sm_scale, cpe_dtype dtype, void* out,
+                                        float* lse, cpe_stream_t stream);
+
+#define CPE_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
  * cpe_get_device_status — synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns CPE_OK, the first device
  * error recorded since the last call (CPE_ERR_TIMEOUT, CPE_ERR_DEVICE_ARG), or

@@ -1,0 +1,68 @@
+"""The allocation-free decode entry point, cpe_decode_attention_noalloc.
+
+Some callers cannot allocate device memory at all: a plugin running inside a
+host program that owns every byte of device memory through its own pool, or a
+serving loop that must not enter an allocator on its hot path (cudaMalloc can
+synchronise the device, and can fail on a fragmented heap).  For them the
+split-KV decode path keeps its partial results in a fixed 8 MiB device array
+that the library declares itself, instead of a workspace the caller would have
+to allocate.
+
+These tests call that entry point through the C ABI and check it against the
+workspace-based cpe_decode_attention, twice in a row (the fixed array is shared
+by every call and keeps the previous call's contents), and check that a batch
+needing more than the fixed array is refused before anything is launched.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests._util import MAX_ABS, REL_RMS, LSE_ABS, check_close, i32, varlen_batch
+
+
+def _lib():
+    from chunked_prefill_extend_gb300 import cpe
+    return cpe
+
+
+def _both_paths(cpe, b):
+    """Append the new rows, then run the workspace path and the fixed-array path."""
+    pl = i32(b["pl"])
+    cpe.cpe_kv_append(b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"], i32(b["qo"]), pl)
+    n, h_q = b["q"].shape[0], b["h_q"]
+    lse_ref = torch.empty(n, h_q, dtype=torch.float32, device="cuda")
+    ref, _ = cpe.cpe_decode_attention(b["q"], b["k_cache"], b["v_cache"], b["page_table"], pl, b["max_kv"],
+                                      lse=lse_ref)
+    out = torch.empty_like(b["q"])
+    lse = torch.empty(n, h_q, dtype=torch.float32, device="cuda")
+    cpe.cpe_decode_attention_noalloc(b["q"], b["k_cache"], b["v_cache"], b["page_table"], pl, b["max_kv"],
+                                     out=out, lse=lse)
+    st, detail = cpe.cpe_get_device_status()
+    assert st == cpe.CPE_OK, f"device status {st} ({detail})"
+    return out, lse, ref, lse_ref
+
+
+@pytest.mark.gpu
+def test_noalloc_decode_matches_workspace_path_twice():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cpe = _lib()
+    # first call: several splits per row; second call: other rows, other sizes
+    first = varlen_batch(901, [(L - 1, 1) for L in (1, 17, 2049, 6000, 9000)], 32, 8, 128)
+    second = varlen_batch(902, [(L - 1, 1) for L in (4097, 33, 12000)], 16, 4, 64)
+    for b in (first, second):
+        out, lse, ref, lse_ref = _both_paths(cpe, b)
+        check_close(out, ref.double().cpu().numpy(), "noalloc vs workspace path", MAX_ABS, REL_RMS)
+        np.testing.assert_allclose(lse.cpu().numpy(), lse_ref.cpu().numpy(), atol=LSE_ABS, rtol=0)
+
+
+def test_noalloc_refuses_batches_above_the_fixed_array():
+    """64 rows x 32 heads x 16 splits x 130 floats needs ~17 MB > 8 MiB: refused on
+    the host with CPE_ERR_CAPACITY, before any device call (the pointers are
+    never dereferenced)."""
+    cpe = _lib()
+    fake = 1 << 20
+    st = cpe._lib.cpe_decode_attention_noalloc(fake, fake, fake, 100000, fake, 2048, fake, 64, 32768, 32, 8, 128,
+                                                16, 0.088, cpe.CPE_BF16, fake, None, None)
+    assert st == cpe.CPE_ERR_CAPACITY
+    assert "8388608" in cpe.cpe_last_error()
