@@ -58,10 +58,19 @@ def chunk_flops(d, h_q, P, E):
 class Chunked:
     """Whole chunked prefill of one request (cfg1/2/3/5)."""
 
-    def __init__(self, spec, device, cpe):
+    def __init__(self, spec, device, cpe, rounds=None):
         self.spec, self.cpe, self.device = spec, cpe, device
         self.req = W.make_chunked(spec, device=device)
         self.chunks, self.cached, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+        self.rounds = rounds or (0, len(self.chunks))
+        if self.rounds[0] > 0:  # the cache must hold every earlier round's keys
+            for c in self.chunks[:self.rounds[0]]:
+                a = c.prefix_len - self.cached
+                cpe.cpe_kv_append(self.req.k[a:a + c.query_len], self.req.v[a:a + c.query_len], self.req.k_cache,
+                                  self.req.v_cache, self.req.page_table,
+                                  torch.tensor([0, c.query_len], dtype=torch.int32, device=device),
+                                  torch.tensor([c.prefix_len], dtype=torch.int32, device=device))
+        self.chunks = self.chunks[self.rounds[0]:self.rounds[1]]
         self.idx = {c.index: (torch.tensor([0, c.query_len], dtype=torch.int32, device=device),
                               torch.tensor([c.prefix_len], dtype=torch.int32, device=device)) for c in self.chunks}
         self.out = torch.empty_like(self.req.q)
@@ -80,7 +89,7 @@ class Chunked:
         v = req.v if v is None else v
         out = self.out if out is None else out
         chunks, _, _ = cpe.cpe_plan_chunks(self.spec.input_len, self.spec.hit_rate, self.spec.chunk)
-        for c in chunks:
+        for c in chunks[self.rounds[0]:self.rounds[1]]:
             qo, pl = self.idx[c.index]
             a = c.prefix_len - self.cached
             cpe.cpe_kv_append(k[a:a + c.query_len], v[a:a + c.query_len], req.k_cache, req.v_cache,
@@ -203,9 +212,14 @@ class Mixed:
         return flops, dt, f"{len(picks)} decode rows x {spec.h_q} heads (all keys)"
 
 
-def make_workload(name, device, cpe):
-    spec = W.CONFIGS[name]
-    return Mixed(spec, device, cpe) if isinstance(spec, W.MixedSpec) else Chunked(spec, device, cpe)
+def make_workload(args, device, cpe):
+    spec = W.CONFIGS[args.workload]
+    if isinstance(spec, W.MixedSpec):
+        return Mixed(spec, device, cpe)
+    if args.input_len:
+        spec = W.shrink(spec, input_len=args.input_len)
+    rounds = tuple(int(x) for x in args.rounds.split(":")) if args.rounds else None
+    return Chunked(spec, device, cpe, rounds)
 
 
 # --------------------------------------------------------------------------- helpers
@@ -291,7 +305,7 @@ def run_ours(args, ws, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     peaks = _peaks()
-    wl = make_workload(args.workload, device, cpe)
+    wl = make_workload(args, device, cpe)
     flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if wl.small else None
     for _ in range(args.warmup):
         wl.step()
@@ -363,7 +377,7 @@ def run_ours(args, ws, rank, local):
         roof["per_chunk_tflops"] = {str(curve[i][0]): round(curve[i][1], 1) for i in pick}
 
     # end to end through the public API with host buffers
-    e2e = e2e_measure(wl, args, device, ws)
+    e2e = None if args.no_e2e else e2e_measure(wl, args, device, ws)
 
     line = {
         "metric": "extend-attn TFLOP/s & tokens/s per chunk; % bf16 TC peak / % HBM BW (1 GB300)",
@@ -371,7 +385,9 @@ def run_ours(args, ws, rank, local):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if W.CONFIGS[args.workload].dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "tokens_per_s": wl.tokens * ws / (ms_per_step * 1e-3),
-        "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}",
+        "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}" +
+                   (f" (input_len {args.input_len})" if args.input_len else "") +
+                   (f" (rounds {args.rounds})" if args.rounds else ""),
                    "l2": "flushed between steps (256 MiB write outside the per-step events)" if flush is not None
                    else "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{ws}", "flops_per_step": wl.flops},
@@ -514,6 +530,9 @@ def main():
     ap.add_argument("--workload", default="cfg5", choices=sorted(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--input-len", type=int, default=0, help="shrink a chunked workload's request (profiling)")
+    ap.add_argument("--rounds", default="", help="a:b, run only chunks [a, b) of a chunked workload (profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":

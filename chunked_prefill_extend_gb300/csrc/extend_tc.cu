@@ -12,10 +12,11 @@
 // per row: the article's online-softmax LSE merge of the two partials, applied
 // tile by tile.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q tile once, then K and V page boxes per key tile
-//               into an NS-stage ring (one box = 16 tokens x 64 dims, 128-byte
-//               swizzle; eight pages stack into one 128-key tile).
+// Warp roles (224 threads):
+//   warps 0, 6  TMA producers: warp 0 the Q tile once and then K, warp 6 V;
+//               page boxes per key tile into NS-stage rings (one box = 16
+//               tokens x 64 dims, 128-byte swizzle; eight pages stack into one
+//               128-key tile).
 //   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
 //               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM.
 //   warps 2-5   softmax: one thread per query row reads its S row from TMEM,
@@ -34,20 +35,20 @@ namespace cpe {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr uint64_t kDrainNs = 2000000000ull;  // fixed bound for the final drain waits
 
 template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;              // 128-byte column blocks per row
   static constexpr int kTileBytes = kBlockM * D * 2;  // 128 rows (or keys) x D bf16
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStages = (D == 128) ? 3 : 6;
   static constexpr int kHalfBytes = 128 * 128;        // 128 rows x 128 bytes
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kSmem = kBarOff + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kSmem = kBarOff + 512 + 1024;  // + barriers + alignment slack
 };
 
 template <int NS>
@@ -110,16 +111,23 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ producers
+    // warp 0 loads Q once and then the K ring, warp 6 the V ring, so neither
+    // stream waits for the other's free slots.
     if (lane == 0) {
-      prefetch_tmap(&a.tm_q);
-      prefetch_tmap(&a.tm_k);
-      prefetch_tmap(&a.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
-      for (int h = 0; h < C::kHalves; ++h)
-        tma_load_3d(smem + C::kQOff + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64,
-                    g * a.group, q0 + i0);
+      const bool is_k = warp == 0;
+      const CUtensorMap* tm = is_k ? &a.tm_k : &a.tm_v;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+      uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
+      prefetch_tmap(tm);
+      if (is_k) {
+        prefetch_tmap(&a.tm_q);
+        mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(smem + C::kQOff + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64, g * a.group, q0 + i0);
+      }
       const int32_t* pt = a.page_table + static_cast<int64_t>(s) * a.max_pages;
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
       int issued = 0;
@@ -138,35 +146,22 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             rows[pg] = pid * kPage;
           }
         }
-        const uint32_t bytes = npg * C::kHalves * (kPage * 128);
-        if (u > 0 && !mbar_wait(&bars->k_empty[st], (u - 1) & 1, abort, a.wait_ns, a.status, kDetailKEmpty))
+        if (u > 0 && !mbar_wait(&empty[st], (u - 1) & 1, abort, a.wait_ns, a.status,
+                                is_k ? kDetailKEmpty : kDetailVEmpty))
           break;
-        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+        mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
         for (int pg = 0; pg < npg; ++pg)
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(smem + C::kKOff + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128),
-                        &a.tm_k, &bars->k_full[st], h * 64, g, rows[pg]);
-        if (u > 0 && !mbar_wait(&bars->v_empty[st], (u - 1) & 1, abort, a.wait_ns, a.status, kDetailVEmpty)) {
-          issued = -(j + 1);  // K of tile j issued, V not
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-        for (int pg = 0; pg < npg; ++pg)
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(smem + C::kVOff + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128),
-                        &a.tm_v, &bars->v_full[st], h * 64, g, rows[pg]);
+            tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64, g,
+                        rows[pg]);
         issued = j + 1;
       }
       // Drain: every copy issued must land before the CTA exits.
       if (*abort) {
-        const int nk = issued >= 0 ? issued : -issued;
-        const int nv = issued >= 0 ? issued : -issued - 1;
         volatile int no_abort = 0;
-        mbar_wait(&bars->q_full, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
-        for (int j = max(0, nk - NS); j < nk; ++j)
-          mbar_wait(&bars->k_full[j % NS], (j / NS) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
-        for (int j = max(0, nv - NS); j < nv; ++j)
-          mbar_wait(&bars->v_full[j % NS], (j / NS) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+        if (is_k) mbar_wait(&bars->q_full, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
+        for (int j = max(0, issued - NS); j < issued; ++j)
+          mbar_wait(&full[j % NS], (j / NS) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
       }
     }
   } else if (warp == 1) {
@@ -233,14 +228,26 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const int b = j & 1;
       if (!mbar_wait(&bars->s_full[b], (j / 2) & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
       tc_fence_after();
+      // the whole S row: four loads in flight, one wait
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      {
+        const uint32_t sa = tmem + lane_base + b * 128;
+        tmem_ld32(sa, r0);
+        tmem_ld32(sa + 32, r1);
+        tmem_ld32(sa + 64, r2);
+        tmem_ld32(sa + 96, r3);
+        tc_wait_ld_dep(r0);
+        reg_dep(r1);
+        reg_dep(r2);
+        reg_dep(r3);
+      }
       float sv[kBlockN];
 #pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld32(tmem + lane_base + b * 128 + c * 32, raw);
-        tc_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) sv[c * 32 + x] = __uint_as_float(raw[x]);
+      for (int x = 0; x < 32; ++x) {
+        sv[x] = __uint_as_float(r0[x]);
+        sv[32 + x] = __uint_as_float(r1[x]);
+        sv[64 + x] = __uint_as_float(r2[x]);
+        sv[96 + x] = __uint_as_float(r3[x]);
       }
       const int kb = j * kBlockN;
       if (kb + kBlockN - 1 > P + i0) {  // tile crosses the diagonal or the end: mask
@@ -248,28 +255,40 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         for (int c = 0; c < kBlockN; ++c)
           if (kb + c > lim) sv[c] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // row max as a tree (16 independent chains)
+      float mx16[16];
 #pragma unroll
-      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
-      const float m_tile = mx * sl2;
+      for (int k = 0; k < 16; ++k) mx16[k] = fmaxf(sv[k], sv[k + 16]);
+#pragma unroll
+      for (int c = 32; c < kBlockN; c += 16)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) mx16[k] = fmaxf(mx16[k], sv[c + k]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) mx16[k] = fmaxf(mx16[k], mx16[k + w]);
+      const float m_tile = mx16[0] * sl2;
       const bool grow = m_tile > m_run + 8.0f;
       const float m_new = grow ? m_tile : m_run;
       const float factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
       m_run = m_new;
       const float mbase = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum = 0.f;
+      float acc[8];
 #pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        uint32_t pk[16];
+      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const float p0 = fast_exp2(fmaf(sv[c * 32 + 2 * x], sl2, -mbase));
-          const float p1 = fast_exp2(fmaf(sv[c * 32 + 2 * x + 1], sl2, -mbase));
-          sum += p0 + p1;
+      for (int c = 0; c < kBlockN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float p0 = fast_exp2(fmaf(sv[c * 64 + 2 * x], sl2, -mbase));
+          const float p1 = fast_exp2(fmaf(sv[c * 64 + 2 * x + 1], sl2, -mbase));
+          acc[x & 7] += p0 + p1;
           pk[x] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + lane_base + b * 128 + c * 16, pk);
+        tmem_st32(tmem + lane_base + b * 128 + c * 32, pk);
       }
+      const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       l_run = l_run * factor + sum;
       tc_wait_st();
       if (j >= 1) {
@@ -278,13 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_fence_after();
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t raw[32];
-            tmem_ld32(tmem + lane_base + 256 + c * 32, raw);
-            tc_wait_ld();
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t o0[32], o1[32];
+            const uint32_t oa = tmem + lane_base + 256 + c * 64;
+            tmem_ld32(oa, o0);
+            tmem_ld32(oa + 32, o1);
+            tc_wait_ld_dep(o0);
+            reg_dep(o1);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * factor);
-            tmem_st32(tmem + lane_base + 256 + c * 32, raw);
+            for (int x = 0; x < 32; ++x) {
+              o0[x] = __float_as_uint(__uint_as_float(o0[x]) * factor);
+              o1[x] = __float_as_uint(__uint_as_float(o1[x]) * factor);
+            }
+            tmem_st32(oa, o0);
+            tmem_st32(oa + 32, o1);
           }
           tc_wait_st();
         }
@@ -306,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       for (int c = 0; c < D / 32; ++c) {
         uint32_t raw[32];
         tmem_ld32(tmem + lane_base + 256 + c * 32, raw);
-        tc_wait_ld();
+        tc_wait_ld_dep(raw);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
