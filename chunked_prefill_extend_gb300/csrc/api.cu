@@ -176,11 +176,13 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   TileEntry* tiles = reinterpret_cast<TileEntry*>(static_cast<uint8_t*>(c.workspace) + L.tiles_off);
   const int n_rows = c.total_q - row_begin;
   const int n_seq = c.n_seqs - seq_begin;
-  const int cap = c.h_kv * ((n_rows + tok - 1) / tok + n_seq);
+  // one CTA per two query tiles (256 rows) of one sequence and KV head
+  const int unit_tok = 2 * tok;
+  const int cap = c.h_kv * ((n_rows + unit_tok - 1) / unit_tok + n_seq);
 
   ScheduleArgs sa{};
   sa.qo_indptr = c.qo_indptr; sa.prefix_len = c.prefix_len; sa.seq_begin = seq_begin; sa.seq_end = c.n_seqs;
-  sa.tok = tok; sa.h_kv = c.h_kv; sa.max_kv_len = c.max_kv_len; sa.max_pages = c.max_pages;
+  sa.tok = unit_tok; sa.h_kv = c.h_kv; sa.max_kv_len = c.max_kv_len; sa.max_pages = c.max_pages;
   sa.capacity = cap; sa.tiles = tiles; sa.status = status;
   e = launch_schedule(sa, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);

@@ -1,8 +1,9 @@
 // Extend attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One CTA computes one work unit: 128 query rows of one sequence that share a
-// KV head (kBlockM / G tokens x the G query heads of the group, so every K/V
-// tile staged in shared memory serves all G heads), against keys [0, kv_end).
+// One CTA computes one work unit: two query tiles of 128 rows of one sequence
+// that share a KV head.  A tile's rows are (128 / G tokens) x (the G query
+// heads of the group), so each K/V tile staged in shared memory serves all G
+// heads of both query tiles: 256 rows per K/V byte brought on chip.
 //
 // Key tiles of 128 are walked in order.  Tiles wholly inside the cached prefix
 // are the unmasked rectangle (Stage 1 of the SGLang chunked-prefill article);
@@ -12,18 +13,26 @@
 // per row: the article's online-softmax LSE merge of the two partials, applied
 // tile by tile.
 //
-// Warp roles (224 threads):
-//   warps 0, 6  TMA producers: warp 0 the Q tile once and then K, warp 6 V;
-//               page boxes per key tile into NS-stage rings (one box = 16
-//               tokens x 64 dims, 128-byte swizzle; eight pages stack into one
-//               128-key tile).
-//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
-//               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM.
-//   warps 2-5   softmax: one thread per query row reads its S row from TMEM,
-//               masks, updates the running max (rescaling O only when the max
-//               grows by more than 2^8), writes P as bf16 over its S columns,
-//               and finally normalises O and stores it.
-// TMEM columns: [0,128) S0, [128,256) S1, [256,256+D) O.
+// Warp roles (384 threads, three warpgroups):
+//   warp 0      TMA producer: both Q tiles once, then the K ring
+//   warp 2      TMA producer: the V ring
+//               (page boxes of 16 tokens x 64 dims, 128-byte swizzle; eight
+//               pages stack into one 128-key tile)
+//   warp 1      TMEM owner and MMA issuer: S_t = Q_t K_j^T into TMEM, and
+//               O_t += P_t V_j with P read from TMEM, for t = 0, 1 in turn, so
+//               the tensor pipe works on one tile while the other's softmax runs
+//   warps 4-7   softmax of query tile 0, warps 8-11 of query tile 1: one thread
+//               per row reads its S row from TMEM, masks, keeps the running max
+//               (rescaling O only when it grows by more than 2^8), writes P as
+//               bf16 over its S columns, and at the end normalises and stores O.
+// The first warpgroup gives registers up (setmaxnreg) to the two softmax
+// warpgroups; the host checks the launch allocation covers the split.
+// TMEM columns: [0,128) S0, [128,256) S1, [256,256+D) O0, [256+D,256+2D) O1.
+//
+// tcgen05.mma instructions from one thread execute in issue order, so S_t for
+// the next key tile may be issued right behind the PV that reads P_t from the
+// same columns; tcgen05.commit tracks every earlier MMA of the thread, so the
+// S barrier also tells the softmax that the previous PV (and thus O_t) is done.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // CPE_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
@@ -35,39 +44,49 @@ namespace cpe {
 
 namespace {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;     // 384 x 168 = 64512 registers at launch
+constexpr int kProducerRegs = 56;    // warpgroup 0 after setmaxnreg.dec
+constexpr int kSoftmaxRegs = 224;    // warpgroups 1, 2 after setmaxnreg.inc
+static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr uint64_t kDrainNs = 2000000000ull;  // fixed bound for the final drain waits
 
 template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;              // 128-byte column blocks per row
   static constexpr int kTileBytes = kBlockM * D * 2;  // 128 rows (or keys) x D bf16
-  static constexpr int kStages = (D == 128) ? 3 : 6;
+  static constexpr int kStagesK = (D == 128) ? 3 : 6;
+  static constexpr int kStagesV = (D == 128) ? 2 : 5;
   static constexpr int kHalfBytes = 128 * 128;        // 128 rows x 128 bytes
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kQOff = 0;                     // two Q tiles
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStagesK * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStagesV * kTileBytes;
   static constexpr int kSmem = kBarOff + 512 + 1024;  // + barriers + alignment slack
 };
 
-template <int NS>
+template <int NK, int NV>
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_full, drain;
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
+__device__ __forceinline__ void setmaxnreg_dec56() { asm volatile("setmaxnreg.dec.sync.aligned.u32 56;"); }
+__device__ __forceinline__ void setmaxnreg_inc224() { asm volatile("setmaxnreg.inc.sync.aligned.u32 224;"); }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendTcArgs a) {
   using C = TcCfg<D>;
-  constexpr int NS = C::kStages;
+  constexpr int NK = C::kStagesK;
+  constexpr int NV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars<NS>* bars = reinterpret_cast<Bars<NS>*>(smem + C::kBarOff);
+  Bars<NK, NV>* bars = reinterpret_cast<Bars<NK, NV>*>(smem + C::kBarOff);
 
   const TileEntry t = a.tiles[blockIdx.x];
   if (t.seq < 0) return;  // unused slot of the tile list (uniform over the CTA)
@@ -79,24 +98,34 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int q0 = a.qo_indptr[s];
   const int E = a.qo_indptr[s + 1] - q0;
   const int P = a.prefix_len[s];
-  const int i0 = t.q_tile * a.tok;
-  const int kv_end = P + min(E, i0 + a.tok);
-  const int n_kt = (kv_end + kBlockN - 1) / kBlockN;
+  // query tile u of this unit starts at token i0[u]; an empty second tile has n_kt = 0
+  int i0[2], n_kt[2], kv_end[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    i0[u] = (2 * t.q_tile + u) * a.tok;
+    kv_end[u] = i0[u] < E ? P + min(E, i0[u] + a.tok) : 0;
+    n_kt[u] = (kv_end[u] + kBlockN - 1) / kBlockN;
+  }
+  const int n_kv = max(n_kt[0], n_kt[1]);
+  const int kv_max = max(kv_end[0], kv_end[1]);
+  const int n_q = n_kt[1] > 0 ? 2 : 1;
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < NK; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < NV; ++i) {
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->o_done[i], 1);
     }
-    mbar_init(&bars->o_full, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -111,30 +140,32 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0 || warp == 6) {
-    // ------------------------------------------------------------ producers
-    // warp 0 loads Q once and then the K ring, warp 6 the V ring, so neither
-    // stream waits for the other's free slots.
-    if (lane == 0) {
+  if (warp < 4) {
+    setmaxnreg_dec56();
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // ---------------------------------------------------------- producers
       const bool is_k = warp == 0;
       const CUtensorMap* tm = is_k ? &a.tm_k : &a.tm_v;
+      const int ns = is_k ? NK : NV;
       uint64_t* full = is_k ? bars->k_full : bars->v_full;
       uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
       prefetch_tmap(tm);
       if (is_k) {
         prefetch_tmap(&a.tm_q);
-        mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(smem + C::kQOff + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64, g * a.group, q0 + i0);
+        mbar_arrive_expect_tx(&bars->q_full, n_q * C::kTileBytes);
+        for (int u = 0; u < n_q; ++u)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(smem + C::kQOff + u * C::kTileBytes + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64,
+                        g * a.group, q0 + i0[u]);
       }
       const int32_t* pt = a.page_table + static_cast<int64_t>(s) * a.max_pages;
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
       int issued = 0;
-      for (int j = 0; j < n_kt; ++j) {
-        const int st = j % NS;
-        const int u = j / NS;
-        const int keys = min(kBlockN, kv_end - j * kBlockN);
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % ns;
+        const int u = j / ns;
+        const int keys = min(kBlockN, kv_max - j * kBlockN);
         const int npg = (keys + kPage - 1) / kPage;
         int rows[kBlockN / kPage];
         for (int pg = 0; pg < npg; ++pg) {
@@ -160,53 +191,64 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       if (*abort) {
         volatile int no_abort = 0;
         if (is_k) mbar_wait(&bars->q_full, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
-        for (int j = max(0, issued - NS); j < issued; ++j)
-          mbar_wait(&full[j % NS], (j / NS) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+        for (int j = max(0, issued - ns); j < issued; ++j)
+          mbar_wait(&full[j % ns], (j / ns) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      const uint32_t sq = smem_u32(smem + C::kQOff);
-      bool ok = mbar_wait(&bars->q_full, 0, abort, a.wait_ns, a.status, kDetailQFull);
-      tc_fence_after();
-      for (int j = 0; ok && j <= n_kt; ++j) {
-        if (j < n_kt) {
-          const int b = j & 1;
-          const int st = j % NS;
-          if (j >= 2 && !mbar_wait(&bars->o_full, (j - 2) & 1, abort, a.wait_ns, a.status, kDetailOFull)) break;
-          if (!mbar_wait(&bars->k_full[st], (j / NS) & 1, abort, a.wait_ns, a.status, kDetailKFull)) break;
-          tc_fence_after();
-          const uint32_t sk = smem_u32(smem + C::kKOff + st * C::kTileBytes);
+      auto issue_s = [&](int u, int st) {
+        const uint32_t sq = smem_u32(smem + C::kQOff + u * C::kTileBytes);
+        const uint32_t sk = smem_u32(smem + C::kKOff + st * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-            tc_mma_ss(tmem + b * 128, smem_desc_sw128(sq + off, 16, 1024),
-                      smem_desc_sw128(sk + off, 16, 1024), idesc_qk, kk > 0);
-          }
-          tc_commit(&bars->k_empty[st]);
-          tc_commit(&bars->s_full[b]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+          tc_mma_ss(tmem + u * 128, smem_desc_sw128(sq + off, 16, 1024), smem_desc_sw128(sk + off, 16, 1024),
+                    idesc_qk, kk > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int b = jj & 1;
-          const int st = jj % NS;
-          if (!mbar_wait(&bars->p_full[b], (jj / 2) & 1, abort, a.wait_ns, a.status, kDetailPFull)) break;
-          if (!mbar_wait(&bars->v_full[st], (jj / NS) & 1, abort, a.wait_ns, a.status, kDetailVFull)) break;
+        tc_commit(&bars->s_full[u]);
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, abort, a.wait_ns, a.status, kDetailQFull) &&
+                mbar_wait(&bars->k_full[0], 0, abort, a.wait_ns, a.status, kDetailKFull);
+      if (ok) {
+        tc_fence_after();
+        for (int u = 0; u < 2; ++u)
+          if (n_kt[u] > 0) issue_s(u, 0);
+        tc_commit(&bars->k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int sv_st = j % NV;
+        const int sk_next = (j + 1) % NK;
+        bool k_next_ready = false;
+        if (!mbar_wait(&bars->v_full[sv_st], (j / NV) & 1, abort, a.wait_ns, a.status, kDetailVFull)) break;
+        for (int u = 0; u < 2 && ok; ++u) {
+          if (j >= n_kt[u]) continue;
+          if (!mbar_wait(&bars->p_full[u], j & 1, abort, a.wait_ns, a.status, kDetailPFull)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sv = smem_u32(smem + C::kVOff + st * C::kTileBytes);
-          const int keys = min(kBlockN, kv_end - jj * kBlockN);
+          const uint32_t sv = smem_u32(smem + C::kVOff + sv_st * C::kTileBytes);
+          const int keys = min(kBlockN, kv_end[u] - j * kBlockN);
           const int nsteps = (keys + 15) / 16;  // only pages that were loaded
-          for (int kk = 0; kk < nsteps; ++kk) {
-            tc_mma_ts(tmem + 256, tmem + b * 128 + kk * 8,
+          for (int kk = 0; kk < nsteps; ++kk)
+            tc_mma_ts(tmem + 256 + u * D, tmem + u * 128 + kk * 8,
                       smem_desc_sw128(sv + kk * (16 * 128), C::kHalfBytes, 1024), idesc_pv,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          if (j + 1 == n_kt[u]) {
+            tc_commit(&bars->o_done[u]);
+          } else {
+            if (!k_next_ready) {
+              if (!mbar_wait(&bars->k_full[sk_next], ((j + 1) / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_next_ready = true;
+            }
+            issue_s(u, sk_next);
           }
-          tc_commit(&bars->v_empty[st]);
-          tc_commit(&bars->o_full);
         }
+        tc_commit(&bars->v_empty[sv_st]);
+        if (k_next_ready) tc_commit(&bars->k_empty[sk_next]);
       }
       // Drain: wait until every MMA issued above has completed.
       tc_commit(&bars->drain);
@@ -214,24 +256,27 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       mbar_wait(&bars->drain, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
     }
   } else {
+    setmaxnreg_inc224();
     // ------------------------------------------------------------ softmax
+    const int u = (warp - 4) / 4;          // query tile of this warpgroup
     const int quad = warp & 3;             // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;        // query row of the tile
-    const int i = i0 + r / a.group;        // token index within the chunk
+    const int i = i0[u] + r / a.group;     // token index within the chunk
     const int lim = P + min(i, E - 1);     // last key this row may see
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_col = u * 128;
+    const uint32_t o_col = 256 + u * D;
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(&bars->s_full[b], (j / 2) & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
+    for (int j = 0; j < n_kt[u]; ++j) {
+      if (!mbar_wait(&bars->s_full[u], j & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
       tc_fence_after();
       // the whole S row: four loads in flight, one wait
       uint32_t r0[32], r1[32], r2[32], r3[32];
       {
-        const uint32_t sa = tmem + lane_base + b * 128;
+        const uint32_t sa = tmem + lane_base + s_col;
         tmem_ld32(sa, r0);
         tmem_ld32(sa + 32, r1);
         tmem_ld32(sa + 64, r2);
@@ -250,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         sv[96 + x] = __uint_as_float(r3[x]);
       }
       const int kb = j * kBlockN;
-      if (kb + kBlockN - 1 > P + i0) {  // tile crosses the diagonal or the end: mask
+      if (kb + kBlockN - 1 > P + i0[u]) {  // tile crosses the diagonal or the end: mask
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c)
           if (kb + c > lim) sv[c] = -INFINITY;
@@ -286,42 +331,37 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           acc[x & 7] += p0 + p1;
           pk[x] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tmem + lane_base + b * 128 + c * 32, pk);
+        tmem_st32(tmem + lane_base + s_col + c * 32, pk);
       }
       const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       l_run = l_run * factor + sum;
-      tc_wait_st();
-      if (j >= 1) {
-        // PV_{j-1} must be complete before O is rescaled or PV_j accumulates.
-        if (!mbar_wait(&bars->o_full, (j - 1) & 1, abort, a.wait_ns, a.status, kDetailOFull)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {
+      // The S barrier fired after every earlier MMA, so O_t holds PV_{j-1}:
+      // rescale it here, before PV_j is issued.
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t o0[32], o1[32];
-            const uint32_t oa = tmem + lane_base + 256 + c * 64;
-            tmem_ld32(oa, o0);
-            tmem_ld32(oa + 32, o1);
-            tc_wait_ld_dep(o0);
-            reg_dep(o1);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o0[32], o1[32];
+          const uint32_t oa = tmem + lane_base + o_col + c * 64;
+          tmem_ld32(oa, o0);
+          tmem_ld32(oa + 32, o1);
+          tc_wait_ld_dep(o0);
+          reg_dep(o1);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              o0[x] = __float_as_uint(__uint_as_float(o0[x]) * factor);
-              o1[x] = __float_as_uint(__uint_as_float(o1[x]) * factor);
-            }
-            tmem_st32(oa, o0);
-            tmem_st32(oa + 32, o1);
+          for (int x = 0; x < 32; ++x) {
+            o0[x] = __float_as_uint(__uint_as_float(o0[x]) * factor);
+            o1[x] = __float_as_uint(__uint_as_float(o1[x]) * factor);
           }
-          tc_wait_st();
+          tmem_st32(oa, o0);
+          tmem_st32(oa + 32, o1);
         }
       }
+      tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+      if (lane == 0) mbar_arrive(&bars->p_full[u]);
     }
-    // epilogue: wait for the last PV, normalise, store
-    if (ok && n_kt > 0 &&
-        mbar_wait(&bars->o_full, (n_kt - 1) & 1, abort, a.wait_ns, a.status, kDetailOFull)) {
+    // epilogue: wait for the last PV of this tile, normalise, store
+    if (ok && n_kt[u] > 0 && mbar_wait(&bars->o_done[u], 0, abort, a.wait_ns, a.status, kDetailOFull)) {
       tc_fence_after();
       const bool valid = i < E;
       const float inv_l = 1.0f / l_run;
@@ -331,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t raw[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, raw);
+        tmem_ld32(tmem + lane_base + o_col + c * 32, raw);
         tc_wait_ld_dep(raw);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -435,8 +475,22 @@ cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+int extend_tc_units_per_cta() { return 2; }
+
+// The softmax warpgroups raise their register limit at run time; that only
+// completes if the launch allocated at least kLaunchRegs per thread.
+template <int D>
+cudaError_t check_regs() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, extend_tc_kernel<D>);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs >= kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s) {
   if (a.n_ctas <= 0) return cudaSuccess;
+  cudaError_t ce = a.d == 128 ? check_regs<128>() : check_regs<64>();
+  if (ce != cudaSuccess) return ce;
   if (a.d == 128) {
     const int smem = TcCfg<128>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
