@@ -199,13 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
       auto issue_s = [&](int u, int st) {
-        const uint32_t sq = smem_u32(smem + C::kQOff + u * C::kTileBytes);
-        const uint32_t sk = smem_u32(smem + C::kKOff + st * C::kTileBytes);
+        const uint64_t qd = smem_desc_sw128(smem_u32(smem + C::kQOff + u * C::kTileBytes), 16, 1024);
+        const uint64_t kd = smem_desc_sw128(smem_u32(smem + C::kKOff + st * C::kTileBytes), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-          tc_mma_ss(tmem + u * 128, smem_desc_sw128(sq + off, 16, 1024), smem_desc_sw128(sk + off, 16, 1024),
-                    idesc_qk, kk > 0);
+          const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4);
+          tc_mma_ss(tmem + u * 128, qd + off, kd + off, idesc_qk, kk > 0);
         }
         tc_commit(&bars->s_full[u]);
       };
@@ -218,37 +217,40 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_commit(&bars->k_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
+        // Both operand stages this iteration needs are waited for up front, so
+        // the MMA bursts below are separated only by the softmax hand-offs.
         const int sv_st = j % NV;
         const int sk_next = (j + 1) % NK;
-        bool k_next_ready = false;
+        const bool more = j + 1 < n_kv;
         if (!mbar_wait(&bars->v_full[sv_st], (j / NV) & 1, abort, a.wait_ns, a.status, kDetailVFull)) break;
-        for (int u = 0; u < 2 && ok; ++u) {
+        if (more && !mbar_wait(&bars->k_full[sk_next], ((j + 1) / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull))
+          break;
+        const uint64_t vdesc = smem_desc_sw128(smem_u32(smem + C::kVOff + sv_st * C::kTileBytes), C::kHalfBytes, 1024);
+        for (int u = 0; u < 2; ++u) {
           if (j >= n_kt[u]) continue;
           if (!mbar_wait(&bars->p_full[u], j & 1, abort, a.wait_ns, a.status, kDetailPFull)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sv = smem_u32(smem + C::kVOff + sv_st * C::kTileBytes);
+          const uint32_t dcol = tmem + 256 + u * D;
+          const uint32_t acol = tmem + u * 128;
           const int keys = min(kBlockN, kv_end[u] - j * kBlockN);
-          const int nsteps = (keys + 15) / 16;  // only pages that were loaded
-          for (int kk = 0; kk < nsteps; ++kk)
-            tc_mma_ts(tmem + 256 + u * D, tmem + u * 128 + kk * 8,
-                      smem_desc_sw128(sv + kk * (16 * 128), C::kHalfBytes, 1024), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          if (j + 1 == n_kt[u]) {
-            tc_commit(&bars->o_done[u]);
+          if (keys == kBlockN) {
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk)
+              tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
           } else {
-            if (!k_next_ready) {
-              if (!mbar_wait(&bars->k_full[sk_next], ((j + 1) / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_next_ready = true;
-            }
-            issue_s(u, sk_next);
+            const int nsteps = (keys + 15) / 16;  // only pages that were loaded
+            for (int kk = 0; kk < nsteps; ++kk)
+              tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
           }
+          if (j + 1 == n_kt[u])
+            tc_commit(&bars->o_done[u]);
+          else
+            issue_s(u, sk_next);
         }
         tc_commit(&bars->v_empty[sv_st]);
-        if (k_next_ready) tc_commit(&bars->k_empty[sk_next]);
+        if (more) tc_commit(&bars->k_empty[sk_next]);
       }
       // Drain: wait until every MMA issued above has completed.
       tc_commit(&bars->drain);
