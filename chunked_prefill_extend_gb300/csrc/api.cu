@@ -86,26 +86,54 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t tiles_off, tiles_bytes, part_o_off, part_ml_off, total;
-  int tile_capacity, max_splits;
+  size_t header_off, units_off, partial_off, part_o_off, part_ml_off, total;
+  int unit_capacity, max_splits, slots;
 };
 
 int group_of(int h_q, int h_kv) { return h_q / h_kv; }
 
+// Workspace: the extend schedule (header, unit list), the partial-result
+// slots of units cut into key-range parts, then the decode split partials.
 Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int max_kv_len) {
   Layout L{};
   const int G = group_of(h_q, h_kv);
-  const int tok = kBlockM / G;
-  const int64_t cap = static_cast<int64_t>(h_kv) * ((total_q + tok - 1) / tok + n_seqs);
-  L.tile_capacity = static_cast<int>(cap);
+  const int unit_tok = 2 * (kBlockM / G);
+  const int64_t cap = static_cast<int64_t>(h_kv) * ((total_q + unit_tok - 1) / unit_tok + n_seqs);
+  L.unit_capacity = static_cast<int>(cap);
   L.max_splits = (max_kv_len + kDecodeSplit - 1) / kDecodeSplit;
-  L.tiles_off = 0;
-  L.tiles_bytes = align256(static_cast<size_t>(cap) * sizeof(TileEntry));
+  L.header_off = 0;
+  L.units_off = 256;
+  L.partial_off = L.units_off + align256(static_cast<size_t>(cap) * sizeof(UnitEntry));
+  L.slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
   const size_t parts = static_cast<size_t>(n_seqs) * h_q * L.max_splits;
-  L.part_o_off = L.tiles_bytes;
+  L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_floats(d) * sizeof(float));
   L.part_ml_off = L.part_o_off + align256(parts * d * sizeof(float));
   L.total = L.part_ml_off + align256(parts * 2 * sizeof(float));
   return L;
+}
+
+ExtendSched sched_of(const Layout& L, void* ws) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  ExtendSched s;
+  s.header = reinterpret_cast<int*>(b + L.header_off);
+  s.units = reinterpret_cast<UnitEntry*>(b + L.units_off);
+  s.partial = reinterpret_cast<float*>(b + L.partial_off);
+  return s;
+}
+
+// SMs of the current device (the persistent extend grid), at most kMaxCtas.
+int persistent_ctas(cudaError_t* err) {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int sms = 0;
+    *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (*err != cudaSuccess) return 0;
+    cache[dev] = sms < kMaxCtas ? sms : kMaxCtas;
+  }
+  return cache[dev];
 }
 
 struct Common {
@@ -173,17 +201,19 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   }
   const int G = group_of(c.h_q, c.h_kv);
   const int tok = kBlockM / G;
-  TileEntry* tiles = reinterpret_cast<TileEntry*>(static_cast<uint8_t*>(c.workspace) + L.tiles_off);
+  const ExtendSched sched = sched_of(L, c.workspace);
   const int n_rows = c.total_q - row_begin;
   const int n_seq = c.n_seqs - seq_begin;
-  // one CTA per two query tiles (256 rows) of one sequence and KV head
+  // units of two query tiles (256 rows) of one sequence and KV head
   const int unit_tok = 2 * tok;
   const int cap = c.h_kv * ((n_rows + unit_tok - 1) / unit_tok + n_seq);
+  const int n_ctas = persistent_ctas(&e);
+  if (n_ctas <= 0) return cuda_fail(fn, e);
 
   ScheduleArgs sa{};
   sa.qo_indptr = c.qo_indptr; sa.prefix_len = c.prefix_len; sa.seq_begin = seq_begin; sa.seq_end = c.n_seqs;
-  sa.tok = unit_tok; sa.h_kv = c.h_kv; sa.max_kv_len = c.max_kv_len; sa.max_pages = c.max_pages;
-  sa.capacity = cap; sa.tiles = tiles; sa.status = status;
+  sa.tok = tok; sa.h_kv = c.h_kv; sa.max_kv_len = c.max_kv_len; sa.max_pages = c.max_pages;
+  sa.capacity = cap; sa.n_ctas = n_ctas; sa.max_slots = L.slots; sa.sched = sched; sa.status = status;
   e = launch_schedule(sa, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 1;
@@ -194,15 +224,16 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
       !make_map(&a.tm_k, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
       !make_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage))
     return fail(CPE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
-  a.page_table = c.page_table; a.qo_indptr = c.qo_indptr; a.prefix_len = c.prefix_len; a.tiles = tiles;
+  a.page_table = c.page_table; a.qo_indptr = c.qo_indptr; a.prefix_len = c.prefix_len; a.sched = sched;
   a.out = c.out; a.lse = c.lse; a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages;
   a.h_q = c.h_q; a.h_kv = c.h_kv; a.group = G; a.tok = tok; a.d = c.d;
   a.scale_log2 = c.sm_scale * 1.4426950408889634f;
   a.wait_ns = static_cast<uint64_t>(g_wait_ns.load() < 0 ? 0 : g_wait_ns.load());
-  a.n_ctas = cap;
+  a.n_ctas = n_ctas;
+  a.max_units = cap;
   e = launch_extend_tc(a, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);
-  g_launches += 1;
+  g_launches += 2;  // the extend kernel and the merge of key-range parts
   return CPE_OK;
 }
 

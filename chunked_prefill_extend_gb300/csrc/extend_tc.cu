@@ -1,20 +1,28 @@
 // Extend attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One CTA computes one work unit: two query tiles of 128 rows of one sequence
-// that share a KV head.  A tile's rows are (128 / G tokens) x (the G query
-// heads of the group), so each K/V tile staged in shared memory serves all G
-// heads of both query tiles: 256 rows per K/V byte brought on chip.
+// Work unit: two query tiles of 128 rows of one sequence that share a KV head.
+// A tile's rows are (128 / G tokens) x (the G query heads of the group), so
+// each K/V tile staged in shared memory serves all G heads of both query
+// tiles: 256 rows per K/V byte brought on chip.
 //
 // Key tiles of 128 are walked in order.  Tiles wholly inside the cached prefix
 // are the unmasked rectangle (Stage 1 of the SGLang chunked-prefill article);
 // tiles that reach the chunk's own keys form the causal triangle (Stage 2),
 // where only the tiles crossing the diagonal apply the mask j <= P + i and
 // tiles above it are never loaded.  Both stages feed one running (m, l, O)
-// per row: the article's online-softmax LSE merge of the two partials, applied
-// tile by tile.
+// per row: the article's online-softmax LSE merge, applied tile by tile.
+//
+// Persistent, balanced grid: one CTA per SM.  The schedule kernel lists the
+// units and cuts each into the same number of key-range parts, chosen so the
+// work items fill whole waves of CTAs; CTAs take items part-major, so the CTAs
+// working on one KV head at a time stream the same key range together (the
+// K/V tiles are read from HBM once and served to the others from L2).  With
+// more than one part, each part's normalised partial (O, m, l) goes to a
+// workspace slot and the merge kernel combines a unit's parts with the same
+// online-softmax LSE rule.
 //
 // Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: both Q tiles once, then the K ring
+//   warp 0      TMA producer: both Q tiles of each unit, then the K ring
 //   warp 2      TMA producer: the V ring
 //               (page boxes of 16 tokens x 64 dims, 128-byte swizzle; eight
 //               pages stack into one 128-key tile)
@@ -28,6 +36,8 @@
 // The first warpgroup gives registers up (setmaxnreg) to the two softmax
 // warpgroups; the host checks the launch allocation covers the split.
 // TMEM columns: [0,128) S0, [128,256) S1, [256,256+D) O0, [256+D,256+2D) O1.
+// Ring stages, S/P phases and the Q buffer advance with running counters that
+// every role keeps identically across the CTA's work items.
 //
 // tcgen05.mma instructions from one thread execute in issue order, so S_t for
 // the next key tile may be issued right behind the PV that reads P_t from the
@@ -46,8 +56,8 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;     // 384 x 168 = 64512 registers at launch
-constexpr int kProducerRegs = 56;    // warpgroup 0 after setmaxnreg.dec
-constexpr int kSoftmaxRegs = 224;    // warpgroups 1, 2 after setmaxnreg.inc
+constexpr int kProducerRegs = 96;    // warpgroup 0 after setmaxnreg.dec
+constexpr int kSoftmaxRegs = 200;    // warpgroups 1, 2 after setmaxnreg.inc
 static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr uint64_t kDrainNs = 2000000000ull;  // fixed bound for the final drain waits
 
@@ -67,7 +77,7 @@ struct TcCfg {
 
 template <int NK, int NV>
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2], o_done[2];
@@ -76,8 +86,40 @@ struct Bars {
   int abort;
 };
 
-__device__ __forceinline__ void setmaxnreg_dec56() { asm volatile("setmaxnreg.dec.sync.aligned.u32 56;"); }
-__device__ __forceinline__ void setmaxnreg_inc224() { asm volatile("setmaxnreg.inc.sync.aligned.u32 224;"); }
+__device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 96;"); }
+__device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 200;"); }
+
+// Work item: key tiles [kv_lo, kv_hi) of one unit.
+struct Item {
+  int seq, g, q0, E, P, kv_lo, kv_hi;
+  int i0[2], kv_end[2], n_kt[2];
+  bool whole;
+};
+
+// Fills `it` for work item i (part i / n_units of unit i % n_units); false if
+// that part is empty (a unit with fewer key tiles than parts).
+__device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, int n_units, int parts, Item& it) {
+  const int u = i % n_units;
+  const int p = i / n_units;
+  const UnitEntry e = a.sched.units[u];
+  const int len = (e.n_kv + parts - 1) / parts;
+  it.kv_lo = p * len;
+  it.kv_hi = min(it.kv_lo + len, e.n_kv);
+  if (it.kv_lo >= it.kv_hi) return false;
+  it.whole = parts == 1;
+  it.seq = e.seq;
+  it.g = e.kv_head;
+  it.q0 = a.qo_indptr[e.seq];
+  it.E = a.qo_indptr[e.seq + 1] - it.q0;
+  it.P = a.prefix_len[e.seq];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    it.i0[t] = (2 * e.pair + t) * a.tok;
+    it.kv_end[t] = it.i0[t] < it.E ? it.P + min(it.E, it.i0[t] + a.tok) : 0;
+    it.n_kt[t] = (it.kv_end[t] + kBlockN - 1) / kBlockN;
+  }
+  return true;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendTcArgs a) {
@@ -88,31 +130,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars<NK, NV>* bars = reinterpret_cast<Bars<NK, NV>*>(smem + C::kBarOff);
 
-  const TileEntry t = a.tiles[blockIdx.x];
-  if (t.seq < 0) return;  // unused slot of the tile list (uniform over the CTA)
+  const int nc = a.sched.header[1];
+  const int n_units = a.sched.header[2];
+  const int parts = a.sched.header[3];
+  const int n_items = n_units * parts;
+  const int cta = blockIdx.x;
+  if (cta >= nc || cta >= n_items) return;  // CTAs without work (uniform over the CTA)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int s = t.seq;
-  const int g = t.kv_head;
-  const int q0 = a.qo_indptr[s];
-  const int E = a.qo_indptr[s + 1] - q0;
-  const int P = a.prefix_len[s];
-  // query tile u of this unit starts at token i0[u]; an empty second tile has n_kt = 0
-  int i0[2], n_kt[2], kv_end[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    i0[u] = (2 * t.q_tile + u) * a.tok;
-    kv_end[u] = i0[u] < E ? P + min(E, i0[u] + a.tok) : 0;
-    n_kt[u] = (kv_end[u] + kBlockN - 1) / kBlockN;
-  }
-  const int n_kv = max(n_kt[0], n_kt[1]);
-  const int kv_max = max(kv_end[0], kv_end[1]);
-  const int n_q = n_kt[1] > 0 ? 2 : 1;
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < NK; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -141,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < 4) {
-    setmaxnreg_dec56();
+    setmaxnreg_dec_producer();
     if ((warp == 0 || warp == 2) && lane == 0) {
       // ---------------------------------------------------------- producers
       const bool is_k = warp == 0;
@@ -151,106 +182,141 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
       prefetch_tmap(tm);
-      if (is_k) {
-        prefetch_tmap(&a.tm_q);
-        mbar_arrive_expect_tx(&bars->q_full, n_q * C::kTileBytes);
-        for (int u = 0; u < n_q; ++u)
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(smem + C::kQOff + u * C::kTileBytes + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64,
-                        g * a.group, q0 + i0[u]);
-      }
-      const int32_t* pt = a.page_table + static_cast<int64_t>(s) * a.max_pages;
+      if (is_k) prefetch_tmap(&a.tm_q);
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % ns;
-        const int u = j / ns;
-        const int keys = min(kBlockN, kv_max - j * kBlockN);
-        const int npg = (keys + kPage - 1) / kPage;
-        int rows[kBlockN / kPage];
-        for (int pg = 0; pg < npg; ++pg) {
-          const int pid = pt[j * (kBlockN / kPage) + pg];
-          if (pid < 0 || pid >= a.num_pages) {
-            record_error(a.status, kStatusDeviceArg, kDetailBadPage);
-            rows[pg] = oob;
-          } else {
-            rows[pg] = pid * kPage;
-          }
+      int cnt = 0;       // ring loads issued so far
+      int items = 0;     // Q loads issued so far
+      bool ok = true;
+      Item it;
+      for (int wi = cta; ok && wi < n_items; wi += nc) {
+        if (!load_item(a, wi, n_units, parts, it)) continue;
+        if (is_k) {
+          if (items > 0 &&
+              !mbar_wait(&bars->q_empty, (items - 1) & 1, abort, a.wait_ns, a.status, kDetailQFull)) break;
+          const int n_q = it.n_kt[1] > 0 ? 2 : 1;
+          mbar_arrive_expect_tx(&bars->q_full, n_q * C::kTileBytes);
+          for (int t = 0; t < n_q; ++t)
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(smem + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64,
+                          it.g * a.group, it.q0 + it.i0[t]);
+          ++items;
         }
-        if (u > 0 && !mbar_wait(&empty[st], (u - 1) & 1, abort, a.wait_ns, a.status,
-                                is_k ? kDetailKEmpty : kDetailVEmpty))
-          break;
-        mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
-        for (int pg = 0; pg < npg; ++pg)
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64, g,
-                        rows[pg]);
-        issued = j + 1;
+        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
+        const int32_t* pt = a.page_table + static_cast<int64_t>(it.seq) * a.max_pages;
+        for (int j = it.kv_lo; j < it.kv_hi; ++j, ++cnt) {
+          const int st = cnt % ns;
+          const int use = cnt / ns;
+          const int keys = min(kBlockN, kv_max - j * kBlockN);
+          const int npg = (keys + kPage - 1) / kPage;
+          int rows[kBlockN / kPage];
+          for (int pg = 0; pg < npg; ++pg) {
+            const int pid = pt[j * (kBlockN / kPage) + pg];
+            if (pid < 0 || pid >= a.num_pages) {
+              record_error(a.status, kStatusDeviceArg, kDetailBadPage);
+              rows[pg] = oob;
+            } else {
+              rows[pg] = pid * kPage;
+            }
+          }
+          if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, abort, a.wait_ns, a.status,
+                                    is_k ? kDetailKEmpty : kDetailVEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
+          for (int pg = 0; pg < npg; ++pg)
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64,
+                          it.g, rows[pg]);
+        }
       }
       // Drain: every copy issued must land before the CTA exits.
       if (*abort) {
         volatile int no_abort = 0;
-        if (is_k) mbar_wait(&bars->q_full, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
-        for (int j = max(0, issued - ns); j < issued; ++j)
-          mbar_wait(&full[j % ns], (j / ns) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+        if (is_k && items > 0) mbar_wait(&bars->q_full, (items - 1) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+        for (int n = max(0, cnt - ns); n < cnt; ++n)
+          mbar_wait(&full[n % ns], (n / ns) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      auto issue_s = [&](int u, int st) {
-        const uint64_t qd = smem_desc_sw128(smem_u32(smem + C::kQOff + u * C::kTileBytes), 16, 1024);
+      auto issue_s = [&](int t, int st) {
+        const uint64_t qd = smem_desc_sw128(smem_u32(smem + C::kQOff + t * C::kTileBytes), 16, 1024);
         const uint64_t kd = smem_desc_sw128(smem_u32(smem + C::kKOff + st * C::kTileBytes), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4);
-          tc_mma_ss(tmem + u * 128, qd + off, kd + off, idesc_qk, kk > 0);
+          tc_mma_ss(tmem + t * 128, qd + off, kd + off, idesc_qk, kk > 0);
         }
-        tc_commit(&bars->s_full[u]);
+        tc_commit(&bars->s_full[t]);
       };
-      bool ok = mbar_wait(&bars->q_full, 0, abort, a.wait_ns, a.status, kDetailQFull) &&
-                mbar_wait(&bars->k_full[0], 0, abort, a.wait_ns, a.status, kDetailKFull);
-      if (ok) {
-        tc_fence_after();
-        for (int u = 0; u < 2; ++u)
-          if (n_kt[u] > 0) issue_s(u, 0);
-        tc_commit(&bars->k_empty[0]);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        // Both operand stages this iteration needs are waited for up front, so
-        // the MMA bursts below are separated only by the softmax hand-offs.
-        const int sv_st = j % NV;
-        const int sk_next = (j + 1) % NK;
-        const bool more = j + 1 < n_kv;
-        if (!mbar_wait(&bars->v_full[sv_st], (j / NV) & 1, abort, a.wait_ns, a.status, kDetailVFull)) break;
-        if (more && !mbar_wait(&bars->k_full[sk_next], ((j + 1) / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull))
+      int kc = 0, vc = 0, items = 0;
+      int pc[2] = {0, 0};
+      bool ok = true;
+      Item it;
+      for (int wi = cta; ok && wi < n_items; wi += nc) {
+        if (!load_item(a, wi, n_units, parts, it)) continue;
+        if (!mbar_wait(&bars->q_full, items & 1, abort, a.wait_ns, a.status, kDetailQFull) ||
+            !mbar_wait(&bars->k_full[kc % NK], (kc / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull)) {
+          ok = false;
           break;
-        const uint64_t vdesc = smem_desc_sw128(smem_u32(smem + C::kVOff + sv_st * C::kTileBytes), C::kHalfBytes, 1024);
-        for (int u = 0; u < 2; ++u) {
-          if (j >= n_kt[u]) continue;
-          if (!mbar_wait(&bars->p_full[u], j & 1, abort, a.wait_ns, a.status, kDetailPFull)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t dcol = tmem + 256 + u * D;
-          const uint32_t acol = tmem + u * 128;
-          const int keys = min(kBlockN, kv_end[u] - j * kBlockN);
-          if (keys == kBlockN) {
-#pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk)
-              tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          } else {
-            const int nsteps = (keys + 15) / 16;  // only pages that were loaded
-            for (int kk = 0; kk < nsteps; ++kk)
-              tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          if (j + 1 == n_kt[u])
-            tc_commit(&bars->o_done[u]);
-          else
-            issue_s(u, sk_next);
         }
-        tc_commit(&bars->v_empty[sv_st]);
-        if (more) tc_commit(&bars->k_empty[sk_next]);
+        ++items;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (it.kv_lo < it.n_kt[t]) issue_s(t, kc % NK);
+        tc_commit(&bars->k_empty[kc % NK]);
+        ++kc;
+        for (int j = it.kv_lo; j < it.kv_hi; ++j) {
+          // Both operand stages this key tile needs are waited for up front, so
+          // the MMA bursts below are separated only by the softmax hand-offs.
+          const int sv_st = vc % NV;
+          const bool more = j + 1 < it.kv_hi;
+          if (!mbar_wait(&bars->v_full[sv_st], (vc / NV) & 1, abort, a.wait_ns, a.status, kDetailVFull) ||
+              (more && !mbar_wait(&bars->k_full[kc % NK], (kc / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull))) {
+            ok = false;
+            break;
+          }
+          const uint64_t vdesc =
+              smem_desc_sw128(smem_u32(smem + C::kVOff + sv_st * C::kTileBytes), C::kHalfBytes, 1024);
+          for (int t = 0; t < 2; ++t) {
+            if (j >= it.n_kt[t]) continue;
+            if (!mbar_wait(&bars->p_full[t], pc[t] & 1, abort, a.wait_ns, a.status, kDetailPFull)) {
+              ok = false;
+              break;
+            }
+            ++pc[t];
+            tc_fence_after();
+            const uint32_t dcol = tmem + 256 + t * D;
+            const uint32_t acol = tmem + t * 128;
+            const int keys = min(kBlockN, it.kv_end[t] - j * kBlockN);
+            const uint32_t first = j > it.kv_lo ? 1u : 0u;
+            if (keys == kBlockN) {
+#pragma unroll
+              for (int kk = 0; kk < kBlockN / 16; ++kk)
+                tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
+                          (first || kk > 0) ? 1u : 0u);
+            } else {
+              const int nsteps = (keys + 15) / 16;  // only pages that were loaded
+              for (int kk = 0; kk < nsteps; ++kk)
+                tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
+                          (first || kk > 0) ? 1u : 0u);
+            }
+            if (j + 1 < min(it.kv_hi, it.n_kt[t]))
+              issue_s(t, kc % NK);
+            else
+              tc_commit(&bars->o_done[t]);
+          }
+          if (!ok) break;
+          tc_commit(&bars->v_empty[sv_st]);
+          ++vc;
+          if (more) {
+            tc_commit(&bars->k_empty[kc % NK]);
+            ++kc;
+          }
+        }
+        tc_commit(&bars->q_empty);  // every S of this item issued: Q may be replaced
       }
       // Drain: wait until every MMA issued above has completed.
       tc_commit(&bars->drain);
@@ -258,138 +324,175 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       mbar_wait(&bars->drain, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
     }
   } else {
-    setmaxnreg_inc224();
+    setmaxnreg_inc_softmax();
     // ------------------------------------------------------------ softmax
-    const int u = (warp - 4) / 4;          // query tile of this warpgroup
+    const int t = (warp - 4) / 4;          // query tile of this warpgroup
     const int quad = warp & 3;             // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;        // query row of the tile
-    const int i = i0[u] + r / a.group;     // token index within the chunk
-    const int lim = P + min(i, E - 1);     // last key this row may see
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_col = u * 128;
-    const uint32_t o_col = 256 + u * D;
+    const uint32_t s_col = t * 128;
+    const uint32_t o_col = 256 + t * D;
     const float sl2 = a.scale_log2;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
+    const size_t slot_floats = partial_slot_floats(D);
+    int sc = 0, od = 0;
     bool ok = true;
-    for (int j = 0; j < n_kt[u]; ++j) {
-      if (!mbar_wait(&bars->s_full[u], j & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
-      tc_fence_after();
-      // the whole S row: four loads in flight, one wait
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      {
-        const uint32_t sa = tmem + lane_base + s_col;
-        tmem_ld32(sa, r0);
-        tmem_ld32(sa + 32, r1);
-        tmem_ld32(sa + 64, r2);
-        tmem_ld32(sa + 96, r3);
-        tc_wait_ld_dep(r0);
-        reg_dep(r1);
-        reg_dep(r2);
-        reg_dep(r3);
+    Item it;
+    for (int wi = cta; ok && wi < n_items; wi += nc) {
+      if (!load_item(a, wi, n_units, parts, it)) continue;
+      const int i = it.i0[t] + r / a.group;       // token index within the chunk
+      const int lim = it.P + min(i, it.E - 1);    // last key this row may see
+      const int jhi = min(it.kv_hi, it.n_kt[t]);
+      const int R = t * kBlockM + r;               // row of the unit
+      float* part = a.sched.partial + static_cast<size_t>(wi) * slot_floats;
+      if (it.kv_lo >= jhi) {
+        // no key tile of this portion reaches this query tile: an empty partial
+        if (!it.whole) {
+          for (int c = 0; c < D; ++c) part[static_cast<size_t>(R) * D + c] = 0.f;
+          part[static_cast<size_t>(kUnitRows) * D + R] = -INFINITY;
+          part[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] = 0.f;
+        }
+        continue;
       }
-      float sv[kBlockN];
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        sv[x] = __uint_as_float(r0[x]);
-        sv[32 + x] = __uint_as_float(r1[x]);
-        sv[64 + x] = __uint_as_float(r2[x]);
-        sv[96 + x] = __uint_as_float(r3[x]);
-      }
-      const int kb = j * kBlockN;
-      if (kb + kBlockN - 1 > P + i0[u]) {  // tile crosses the diagonal or the end: mask
-#pragma unroll
-        for (int c = 0; c < kBlockN; ++c)
-          if (kb + c > lim) sv[c] = -INFINITY;
-      }
-      // row max as a tree (16 independent chains)
-      float mx16[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) mx16[k] = fmaxf(sv[k], sv[k + 16]);
-#pragma unroll
-      for (int c = 32; c < kBlockN; c += 16)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) mx16[k] = fmaxf(mx16[k], sv[c + k]);
-#pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int k = 0; k < w; ++k) mx16[k] = fmaxf(mx16[k], mx16[k + w]);
-      const float m_tile = mx16[0] * sl2;
-      const bool grow = m_tile > m_run + 8.0f;
-      const float m_new = grow ? m_tile : m_run;
-      const float factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
-      m_run = m_new;
-      const float mbase = (m_run == -INFINITY) ? 0.f : m_run;
-      float acc[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBlockN / 64; ++c) {
-        uint32_t pk[32];
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      for (int j = it.kv_lo; j < jhi; ++j) {
+        if (!mbar_wait(&bars->s_full[t], sc & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
+        ++sc;
+        tc_fence_after();
+        // the whole S row: four loads in flight, one wait
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        {
+          const uint32_t sa = tmem + lane_base + s_col;
+          tmem_ld32(sa, r0);
+          tmem_ld32(sa + 32, r1);
+          tmem_ld32(sa + 64, r2);
+          tmem_ld32(sa + 96, r3);
+          tc_wait_ld_dep(r0);
+          reg_dep(r1);
+          reg_dep(r2);
+          reg_dep(r3);
+        }
+        float sv[kBlockN];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float p0 = fast_exp2(fmaf(sv[c * 64 + 2 * x], sl2, -mbase));
-          const float p1 = fast_exp2(fmaf(sv[c * 64 + 2 * x + 1], sl2, -mbase));
-          acc[x & 7] += p0 + p1;
-          pk[x] = pack_bf16x2(p0, p1);
+          sv[x] = __uint_as_float(r0[x]);
+          sv[32 + x] = __uint_as_float(r1[x]);
+          sv[64 + x] = __uint_as_float(r2[x]);
+          sv[96 + x] = __uint_as_float(r3[x]);
         }
-        tmem_st32(tmem + lane_base + s_col + c * 32, pk);
-      }
-      const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      l_run = l_run * factor + sum;
-      // The S barrier fired after every earlier MMA, so O_t holds PV_{j-1}:
-      // rescale it here, before PV_j is issued.
-      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+        const int kb = j * kBlockN;
+        if (kb + kBlockN - 1 > it.P + it.i0[t]) {  // tile crosses the diagonal or the end: mask
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t o0[32], o1[32];
-          const uint32_t oa = tmem + lane_base + o_col + c * 64;
-          tmem_ld32(oa, o0);
-          tmem_ld32(oa + 32, o1);
-          tc_wait_ld_dep(o0);
-          reg_dep(o1);
+          for (int c = 0; c < kBlockN; ++c)
+            if (kb + c > lim) sv[c] = -INFINITY;
+        }
+        // row max as a tree (16 independent chains)
+        float mx16[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) mx16[q] = fmaxf(sv[q], sv[q + 16]);
+#pragma unroll
+        for (int c = 32; c < kBlockN; c += 16)
+#pragma unroll
+          for (int q = 0; q < 16; ++q) mx16[q] = fmaxf(mx16[q], sv[c + q]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int q = 0; q < w; ++q) mx16[q] = fmaxf(mx16[q], mx16[q + w]);
+        const float m_tile = mx16[0] * sl2;
+        const bool grow = m_tile > m_run + 8.0f;
+        const float m_new = grow ? m_tile : m_run;
+        const float factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
+        m_run = m_new;
+        const float mbase = (m_run == -INFINITY) ? 0.f : m_run;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kBlockN / 64; ++c) {
+          uint32_t pk[32];
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
-            o0[x] = __float_as_uint(__uint_as_float(o0[x]) * factor);
-            o1[x] = __float_as_uint(__uint_as_float(o1[x]) * factor);
+            const float p0 = fast_exp2(fmaf(sv[c * 64 + 2 * x], sl2, -mbase));
+            const float p1 = fast_exp2(fmaf(sv[c * 64 + 2 * x + 1], sl2, -mbase));
+            acc[x & 7] += p0 + p1;
+            pk[x] = pack_bf16x2(p0, p1);
           }
-          tmem_st32(oa, o0);
-          tmem_st32(oa + 32, o1);
+          tmem_st32(tmem + lane_base + s_col + c * 32, pk);
         }
+        const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        l_run = l_run * factor + sum;
+        // The S barrier fired after every earlier MMA, so O_t holds the previous
+        // PV: rescale it here, before the next PV is issued.
+        if (j > it.kv_lo && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t o0[32], o1[32];
+            const uint32_t oa = tmem + lane_base + o_col + c * 64;
+            tmem_ld32(oa, o0);
+            tmem_ld32(oa + 32, o1);
+            tc_wait_ld_dep(o0);
+            reg_dep(o1);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              o0[x] = __float_as_uint(__uint_as_float(o0[x]) * factor);
+              o1[x] = __float_as_uint(__uint_as_float(o1[x]) * factor);
+            }
+            tmem_st32(oa, o0);
+            tmem_st32(oa + 32, o1);
+          }
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[t]);
       }
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[u]);
-    }
-    // epilogue: wait for the last PV of this tile, normalise, store
-    if (ok && n_kt[u] > 0 && mbar_wait(&bars->o_done[u], 0, abort, a.wait_ns, a.status, kDetailOFull)) {
+      if (!ok) break;
+      // epilogue: wait for the last PV of this tile, normalise, store
+      if (!mbar_wait(&bars->o_done[t], od & 1, abort, a.wait_ns, a.status, kDetailOFull)) { ok = false; break; }
+      ++od;
       tc_fence_after();
-      const bool valid = i < E;
       const float inv_l = 1.0f / l_run;
-      const int head = g * a.group + r % a.group;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
-                            (static_cast<int64_t>(q0 + i) * a.h_q + head) * D;
+      if (it.whole) {
+        const bool valid = i < it.E;
+        const int head = it.g * a.group + r % a.group;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                              (static_cast<int64_t>(it.q0 + i) * a.h_q + head) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld32(tmem + lane_base + o_col + c * 32, raw);
-        tc_wait_ld_dep(raw);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(tmem + lane_base + o_col + c * 32, raw);
+          tc_wait_ld_dep(raw);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(raw[8 * x + 0]) * inv_l, __uint_as_float(raw[8 * x + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(raw[8 * x + 2]) * inv_l, __uint_as_float(raw[8 * x + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(raw[8 * x + 4]) * inv_l, __uint_as_float(raw[8 * x + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(raw[8 * x + 6]) * inv_l, __uint_as_float(raw[8 * x + 7]) * inv_l);
-            dst[x] = v;
+            for (int x = 0; x < 4; ++x) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(raw[8 * x + 0]) * inv_l, __uint_as_float(raw[8 * x + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(raw[8 * x + 2]) * inv_l, __uint_as_float(raw[8 * x + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(raw[8 * x + 4]) * inv_l, __uint_as_float(raw[8 * x + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(raw[8 * x + 6]) * inv_l, __uint_as_float(raw[8 * x + 7]) * inv_l);
+              dst[x] = v;
+            }
           }
         }
+        if (valid && a.lse != nullptr)
+          a.lse[static_cast<int64_t>(it.q0 + i) * a.h_q + head] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      } else {
+        // one part of a unit: the normalised partial goes to the item's slot
+        float4* prow = reinterpret_cast<float4*>(part + static_cast<size_t>(R) * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(tmem + lane_base + o_col + c * 32, raw);
+          tc_wait_ld_dep(raw);
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            prow[c * 8 + x] = make_float4(__uint_as_float(raw[4 * x]) * inv_l, __uint_as_float(raw[4 * x + 1]) * inv_l,
+                                          __uint_as_float(raw[4 * x + 2]) * inv_l, __uint_as_float(raw[4 * x + 3]) * inv_l);
+        }
+        part[static_cast<size_t>(kUnitRows) * D + R] = m_run;
+        part[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] = l_run;
       }
-      if (valid && a.lse != nullptr)
-        a.lse[static_cast<int64_t>(q0 + i) * a.h_q + head] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
     }
   }
 
@@ -399,6 +502,65 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Combine the parts of each unit (the online-softmax LSE rule) and write the
+// unit's rows.  Block b takes unit b; 256 threads, one row each.
+template <int D>
+__global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant__ ExtendTcArgs a) {
+  const int n_units = a.sched.header[2];
+  const int parts = a.sched.header[3];
+  const int u = blockIdx.x;
+  if (parts <= 1 || u >= n_units) return;
+  const UnitEntry e = a.sched.units[u];
+  const int len = (e.n_kv + parts - 1) / parts;
+  const int R = threadIdx.x;
+  const int t = R / kBlockM;
+  const int r = R % kBlockM;
+  const int q0 = a.qo_indptr[e.seq];
+  const int E = a.qo_indptr[e.seq + 1] - q0;
+  const int i = (2 * e.pair + t) * a.tok + r / a.group;
+  if (i >= E) return;
+  const size_t slot_floats = partial_slot_floats(D);
+  float M = -INFINITY;
+  for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
+    const float* sl = a.sched.partial + static_cast<size_t>(p * n_units + u) * slot_floats;
+    if (sl[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] > 0.f)
+      M = fmaxf(M, sl[static_cast<size_t>(kUnitRows) * D + R]);
+  }
+  float wsum = 0.f;
+  float o[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) o[d] = 0.f;
+  for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
+    const float* sl = a.sched.partial + static_cast<size_t>(p * n_units + u) * slot_floats;
+    const float l = sl[static_cast<size_t>(kUnitRows) * D + kUnitRows + R];
+    if (!(l > 0.f)) continue;  // this part holds no key of this row
+    const float w = fast_exp2(sl[static_cast<size_t>(kUnitRows) * D + R] - M) * l;
+    wsum += w;
+    const float4* row = reinterpret_cast<const float4*>(sl + static_cast<size_t>(R) * D);
+#pragma unroll
+    for (int d4 = 0; d4 < D / 4; ++d4) {
+      const float4 v = row[d4];
+      o[4 * d4] += w * v.x;
+      o[4 * d4 + 1] += w * v.y;
+      o[4 * d4 + 2] += w * v.z;
+      o[4 * d4 + 3] += w * v.w;
+    }
+  }
+  const float inv = 1.f / wsum;
+  const int head = e.kv_head * a.group + r % a.group;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(q0 + i) * a.h_q + head) * D);
+#pragma unroll
+  for (int x = 0; x < D / 8; ++x) {
+    uint4 v;
+    v.x = pack_bf16x2(o[8 * x + 0] * inv, o[8 * x + 1] * inv);
+    v.y = pack_bf16x2(o[8 * x + 2] * inv, o[8 * x + 3] * inv);
+    v.z = pack_bf16x2(o[8 * x + 4] * inv, o[8 * x + 5] * inv);
+    v.w = pack_bf16x2(o[8 * x + 6] * inv, o[8 * x + 7] * inv);
+    dst[x] = v;
+  }
+  if (a.lse != nullptr) a.lse[static_cast<int64_t>(q0 + i) * a.h_q + head] = (M + __log2f(wsum)) * 0.69314718055994531f;
 }
 
 // Block-wide exclusive prefix sum (blockDim.x a multiple of 32, <= 1024).
@@ -430,6 +592,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
   return base + x - v;
 }
 
+// Query tiles of sequence s (0 if its lengths are out of range).
 __device__ int seq_tiles(const ScheduleArgs& a, int s, bool record) {
   const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
   const int P = a.prefix_len[s];
@@ -439,31 +602,64 @@ __device__ int seq_tiles(const ScheduleArgs& a, int s, bool record) {
   return bad ? 0 : (E + a.tok - 1) / a.tok;
 }
 
-// Tile list: for each KV head, each sequence's query tiles, last tile first
-// (the last tiles see the most keys).  Slots past the real count get seq = -1.
+// Unit list (per KV head, each sequence's units last-first) and the number of
+// key-range parts per unit.
 __global__ void schedule_kernel(ScheduleArgs a) {
   __shared__ int warp_sums[32];
   const int n = a.seq_end - a.seq_begin;
   int local = 0;
-  for (int k = threadIdx.x; k < n; k += blockDim.x) local += seq_tiles(a, a.seq_begin + k, true);
-  int total = 0;
-  block_exclusive_scan(local, &total, warp_sums);
+  for (int k = threadIdx.x; k < n; k += blockDim.x) local += (seq_tiles(a, a.seq_begin + k, true) + 1) / 2;
+  int pairs = 0;  // units per KV head
+  block_exclusive_scan(local, &pairs, warp_sums);
+  const int n_units = min(pairs * a.h_kv, a.capacity);
+  if (pairs * a.h_kv > a.capacity && threadIdx.x == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
   int carry = 0;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     const int k = c0 + threadIdx.x;
     const int s = a.seq_begin + k;
-    const int cnt = k < n ? seq_tiles(a, s, false) : 0;
+    const int np = k < n ? (seq_tiles(a, s, false) + 1) / 2 : 0;
     int chunk_total = 0;
-    const int off = carry + block_exclusive_scan(cnt, &chunk_total, warp_sums);
-    for (int g = 0; g < a.h_kv; ++g)
-      for (int q = 0; q < cnt; ++q) {
-        const int idx = g * total + off + q;
-        if (idx < a.capacity) a.tiles[idx] = TileEntry{s, cnt - 1 - q, g, 0};
+    const int off = carry + block_exclusive_scan(np, &chunk_total, warp_sums);
+    if (np > 0) {
+      const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
+      const int P = a.prefix_len[s];
+      for (int q = 0; q < np; ++q) {
+        const int pair = np - 1 - q;
+        const int i_last = min(E, (2 * pair + 2) * a.tok);  // tokens [0, i_last) of the unit's rows
+        const int n_kv = (P + i_last + kBlockN - 1) / kBlockN;
+        for (int g = 0; g < a.h_kv; ++g) {
+          const int idx = g * pairs + off + q;
+          if (idx < a.capacity) a.sched.units[idx] = UnitEntry{s, pair, g, n_kv};
+        }
       }
+    }
     carry += chunk_total;
   }
-  for (int idx = total * a.h_kv + threadIdx.x; idx < a.capacity; idx += blockDim.x)
-    a.tiles[idx] = TileEntry{-1, 0, 0, 0};
+  __syncthreads();
+  // total key tiles, then the number of parts per unit: whole waves of CTAs
+  int wl = 0;
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) wl += a.sched.units[u].n_kv;
+  int W = 0;
+  block_exclusive_scan(wl, &W, warp_sums);
+  if (threadIdx.x == 0) {
+    int best = 1;
+    float best_eff = 0.f;
+    for (int p = 1; p <= kMaxParts; ++p) {
+      if (p > 1 && (p * n_units > a.max_slots || W < p * n_units * kMinTilesPerPart)) break;
+      const int items = p * n_units;
+      const int ncp = min(a.n_ctas, items);
+      const int waves = (items + ncp - 1) / ncp;
+      const float eff = static_cast<float>(items) / static_cast<float>(waves * ncp);
+      if (eff > best_eff + 0.03f) {  // more parts only when they fill the waves clearly better
+        best = p;
+        best_eff = eff;
+      }
+    }
+    a.sched.header[0] = W;
+    a.sched.header[1] = n_units > 0 ? min(a.n_ctas, best * n_units) : 0;
+    a.sched.header[2] = n_units;
+    a.sched.header[3] = best;
+  }
 }
 
 }  // namespace
@@ -476,8 +672,6 @@ cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
   schedule_kernel<<<1, 1024, 0, s>>>(a);
   return cudaGetLastError();
 }
-
-int extend_tc_units_per_cta() { return 2; }
 
 // The softmax warpgroups raise their register limit at run time; that only
 // completes if the launch allocated at least kLaunchRegs per thread.
@@ -498,11 +692,17 @@ cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     extend_tc_kernel<128><<<a.n_ctas, kThreads, smem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    extend_merge_kernel<128><<<a.max_units, 256, 0, s>>>(a);
   } else {
     const int smem = TcCfg<64>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     extend_tc_kernel<64><<<a.n_ctas, kThreads, smem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    extend_merge_kernel<64><<<a.max_units, 256, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

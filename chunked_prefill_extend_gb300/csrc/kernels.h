@@ -13,23 +13,42 @@ constexpr int kBlockN = 128;   // keys per extend K/V tile
 constexpr int kPage = 16;      // page size (tokens)
 constexpr int kDecodeSplit = 2048;  // keys per decode split
 
-struct TileEntry {  // one extend work unit
+constexpr int kMaxCtas = 160;        // upper bound of the persistent extend grid (SMs used)
+constexpr int kMaxParts = 8;         // key-range parts a unit may be cut into
+constexpr int kMinTilesPerPart = 4;  // parts shorter than this (on average) are not used
+constexpr int kMaxSlots = 1024;      // partial-result slots in the workspace
+constexpr int kUnitRows = 2 * kBlockM;
+
+struct UnitEntry {  // one extend work unit: two query tiles of one sequence and KV head
   int seq;
-  int q_tile;
+  int pair;      // query tiles 2*pair and 2*pair+1 of the sequence
   int kv_head;
-  int pad;
+  int n_kv;      // key tiles the unit needs
 };
+
+// Device-side schedule kept in the caller's workspace.  Work item i is part
+// p = i / n_units of unit u = i % n_units: key tiles [p*len, min((p+1)*len, n_kv))
+// with len = ceil(n_kv / parts).  CTA c takes items c, c + n_ctas, ...
+struct ExtendSched {
+  int* header;          // [0] total key tiles, [1] CTAs used, [2] units, [3] parts per unit
+  UnitEntry* units;     // [capacity]
+  float* partial;       // [parts * units] slots: O [256 x d] (normalised), m [256] (log2), l [256]
+};
+
+__host__ __device__ constexpr size_t partial_slot_floats(int d) { return size_t(kUnitRows) * d + 2 * kUnitRows; }
 
 struct ScheduleArgs {
   const int32_t* qo_indptr;
   const int32_t* prefix_len;
   int seq_begin, seq_end;   // sequences [seq_begin, seq_end) take part
-  int tok;                  // tokens per tile (kBlockM / G)
+  int tok;                  // tokens per query tile (kBlockM / G)
   int h_kv;
   int max_kv_len;
   int max_pages;
-  int capacity;             // entries in `tiles` (the launch's grid size)
-  TileEntry* tiles;
+  int capacity;             // unit entries available
+  int n_ctas;               // persistent grid size
+  int max_slots;            // partial slots available
+  ExtendSched sched;
   int* status;
 };
 
@@ -38,7 +57,7 @@ struct ExtendTcArgs {
   const int32_t* page_table;
   const int32_t* qo_indptr;
   const int32_t* prefix_len;
-  const TileEntry* tiles;
+  ExtendSched sched;
   void* out;
   float* lse;
   int* status;
@@ -48,6 +67,7 @@ struct ExtendTcArgs {
   float scale_log2;
   uint64_t wait_ns;
   int n_ctas;
+  int max_units;  // unit capacity (the merge kernel's grid)
 };
 
 struct ExtendSimtArgs {
@@ -97,7 +117,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s);
-cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s);
+cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s);  // + the merge of split units
 cudaError_t launch_extend_simt(const ExtendSimtArgs& a, cudaStream_t s);
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
