@@ -386,40 +386,45 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           for (int c = 0; c < kBlockN; ++c)
             if (kb + c > lim) sv[c] = -INFINITY;
         }
-        // row max as a tree (16 independent chains)
-        float mx16[16];
+        // row max: 16 independent chains of 3-input maxes, then a tree
+        float mx[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) mx16[q] = fmaxf(sv[q], sv[q + 16]);
+        for (int q = 0; q < 16; ++q) {
+          mx[q] = fmax3(sv[q], sv[q + 16], sv[q + 32]);
+          mx[q] = fmax3(mx[q], sv[q + 48], sv[q + 64]);
+          mx[q] = fmax3(mx[q], sv[q + 80], sv[q + 96]);
+          mx[q] = fmaxf(mx[q], sv[q + 112]);
+        }
 #pragma unroll
-        for (int c = 32; c < kBlockN; c += 16)
-#pragma unroll
-          for (int q = 0; q < 16; ++q) mx16[q] = fmaxf(mx16[q], sv[c + q]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int q = 0; q < w; ++q) mx16[q] = fmaxf(mx16[q], mx16[q + w]);
-        const float m_tile = mx16[0] * sl2;
+        for (int q = 0; q < 5; ++q) mx[q] = fmax3(mx[q], mx[q + 5], mx[q + 10]);
+        const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmaxf(mx[3], mx[4]), mx[15]) * sl2;
         const bool grow = m_tile > m_run + 8.0f;
         const float m_new = grow ? m_tile : m_run;
         const float factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
         m_run = m_new;
         const float mbase = (m_run == -INFINITY) ? 0.f : m_run;
-        float acc[8];
+        // p = 2^(s * scale * log2 e - m): scale-and-subtract and the row sum on pairs
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 negm = make_float2(-mbase, -mbase);
+        float2 acc[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kBlockN / 64; ++c) {
           uint32_t pk[32];
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
-            const float p0 = fast_exp2(fmaf(sv[c * 64 + 2 * x], sl2, -mbase));
-            const float p1 = fast_exp2(fmaf(sv[c * 64 + 2 * x + 1], sl2, -mbase));
-            acc[x & 7] += p0 + p1;
-            pk[x] = pack_bf16x2(p0, p1);
+            const float2 z = __ffma2_rn(make_float2(sv[c * 64 + 2 * x], sv[c * 64 + 2 * x + 1]), sl2x2, negm);
+            const float2 pp = make_float2(fast_exp2(z.x), fast_exp2(z.y));
+            acc[x & 3] = __fadd2_rn(acc[x & 3], pp);
+            pk[x] = pack_bf16x2(pp.x, pp.y);
           }
           tmem_st32(tmem + lane_base + s_col + c * 32, pk);
         }
-        const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+        const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a03 = __fadd2_rn(a01, a23);
+        const float sum = a03.x + a03.y;
         l_run = l_run * factor + sum;
         // The S barrier fired after every earlier MMA, so O_t holds the previous
         // PV: rescale it here, before the next PV is issued.
