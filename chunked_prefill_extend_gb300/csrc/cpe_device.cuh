@@ -90,15 +90,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep in the barrier until
+// the phase completes (or the hint expires) instead of spinning, leaving the
+// issue slots of its sub-partition to the warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up when
 // `*abort` becomes non-zero or after `limit_ns` nanoseconds: then it records a
 // timeout in the status word, raises the CTA's abort flag and returns false.
+// A zero limit gives up at the first unsatisfied poll.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns, int* status, int detail) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns > 0 && mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 >= limit_ns) {
       record_error(status, kStatusTimeout, detail);
