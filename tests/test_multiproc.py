@@ -1,0 +1,61 @@
+"""The benchmark's multi-process path on CPU (world size 2, gloo).
+
+Each GPU runs an independent replica of the workload (the path partitions
+into independent sequences and heads, so there is no data-path collective);
+the only cross-rank steps are the barrier around the timed region and the
+max-over-ranks of the elapsed time.  These run here with gloo.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE="2", RANK=str(rank),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    ws, r, local = bench.dist_setup()
+    bench.barrier(ws)
+    got = bench.max_over_ranks(10.0 * (rank + 1) + 0.25, ws, "cpu")
+    bench.barrier(ws)
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump({"ws": ws, "rank": r, "max": got}, f)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_barrier_and_max_over_ranks_gloo(tmp_path):
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(port, str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)]
+    assert [x["rank"] for x in res] == [0, 1]
+    assert all(x["ws"] == 2 for x in res)
+    assert all(x["max"] == 20.25 for x in res)  # every rank sees the slowest rank's time
+
+
+def test_reference_arm_prints_one_line_from_rank0_only():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--workload", "cfg4", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
