@@ -271,6 +271,8 @@ class Mixed:
 def make_workload(args, device, cpe):
     spec = W.CONFIGS[args.workload]
     if isinstance(spec, W.MixedSpec):
+        if args.decode_rows:
+            spec = W.shrink(spec, n_decode=args.decode_rows)
         return Mixed(spec, device, cpe)
     if args.input_len:
         spec = W.shrink(spec, input_len=args.input_len)
@@ -445,6 +447,7 @@ def run_ours(args, ws, rank, local):
         "tokens_per_s": wl.tokens * ws / (ms_per_step * 1e-3),
         "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}" +
                    (f" (input_len {args.input_len})" if args.input_len else "") +
+                   (f" (decode rows {args.decode_rows})" if args.decode_rows else "") +
                    (f" (rounds {args.rounds})" if args.rounds else ""),
                    "l2": "flushed between steps (256 MiB write outside the per-step events)" if flush is not None
                    else "inputs larger than L2 (no flush)",
@@ -598,6 +601,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     ap.add_argument("--input-len", type=int, default=0, help="shrink a chunked workload's request (profiling)")
+    ap.add_argument("--decode-rows", type=int, default=0, help="shrink the mixed step's decode rows (profiling)")
     ap.add_argument("--rounds", default="", help="a:b, run only chunks [a, b) of a chunked workload (profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
