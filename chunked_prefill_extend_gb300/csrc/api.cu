@@ -222,7 +222,9 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   std::memset(&a, 0, sizeof a);
   if (!make_map(&a.tm_q, c.q, c.d, c.h_q, c.total_q, G, tok) ||
       !make_map(&a.tm_k, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
-      !make_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage))
+      !make_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
+      !make_map(&a.tm_k128, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
+      !make_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN))
     return fail(CPE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
   a.page_table = c.page_table; a.qo_indptr = c.qo_indptr; a.prefix_len = c.prefix_len; a.sched = sched;
   a.out = c.out; a.lse = c.lse; a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages;

@@ -25,7 +25,9 @@
 //   warp 0      TMA producer: both Q tiles of each unit, then the K ring
 //   warp 2      TMA producer: the V ring
 //               (page boxes of 16 tokens x 64 dims, 128-byte swizzle; eight
-//               pages stack into one 128-key tile)
+//               pages stack into one 128-key tile; when the eight pages are
+//               consecutive in the cache one 128-token box per 64-dim half
+//               replaces the sixteen page boxes)
 //   warp 1      TMEM owner and MMA issuer: S_t = Q_t K_j^T into TMEM, and
 //               O_t += P_t V_j with P read from TMEM, for t = 0, 1 in turn, so
 //               the tensor pipe works on one tile while the other's softmax runs
@@ -177,11 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       // ---------------------------------------------------------- producers
       const bool is_k = warp == 0;
       const CUtensorMap* tm = is_k ? &a.tm_k : &a.tm_v;
+      const CUtensorMap* tm128 = is_k ? &a.tm_k128 : &a.tm_v128;
       const int ns = is_k ? NK : NV;
       uint64_t* full = is_k ? bars->k_full : bars->v_full;
       uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
       prefetch_tmap(tm);
+      prefetch_tmap(tm128);
       if (is_k) prefetch_tmap(&a.tm_q);
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
       int cnt = 0;       // ring loads issued so far
@@ -209,13 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           const int keys = min(kBlockN, kv_max - j * kBlockN);
           const int npg = (keys + kPage - 1) / kPage;
           int rows[kBlockN / kPage];
+          bool contiguous = npg == kBlockN / kPage;  // eight pages back to back: one box per half
           for (int pg = 0; pg < npg; ++pg) {
             const int pid = pt[j * (kBlockN / kPage) + pg];
             if (pid < 0 || pid >= a.num_pages) {
               record_error(a.status, kStatusDeviceArg, kDetailBadPage);
               rows[pg] = oob;
+              contiguous = false;
             } else {
               rows[pg] = pid * kPage;
+              contiguous = contiguous && rows[pg] == rows[0] + pg * kPage;
             }
           }
           if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, abort, a.wait_ns, a.status,
@@ -224,10 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             break;
           }
           mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
-          for (int pg = 0; pg < npg; ++pg)
+          if (contiguous) {
             for (int h = 0; h < C::kHalves; ++h)
-              tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64,
-                          it.g, rows[pg]);
+              tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes, tm128, &full[st], h * 64, it.g, rows[0]);
+          } else {
+            for (int pg = 0; pg < npg; ++pg)
+              for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64,
+                            it.g, rows[pg]);
+          }
         }
       }
       // Drain: every copy issued must land before the CTA exits.

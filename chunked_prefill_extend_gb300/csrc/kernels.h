@@ -54,6 +54,7 @@ struct ScheduleArgs {
 
 struct ExtendTcArgs {
   CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_k128, tm_v128;  // the same caches with 128-token boxes (8 consecutive pages)
   const int32_t* page_table;
   const int32_t* qo_indptr;
   const int32_t* prefix_len;
