@@ -90,6 +90,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Three non-blocking phase tests issued back to back (their latencies overlap);
+// bit i of the result is set when barrier i's phase with parity i completed.
+__device__ __forceinline__ uint32_t mbar_test3(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                               uint32_t p2) {
+  uint32_t r0, r1, r2;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%5], %6;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%7], %8;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t"
+      "selp.u32 %1, 2, 0, q1;\n\t"
+      "selp.u32 %2, 4, 0, q2;\n\t}"
+      : "=r"(r0), "=r"(r1), "=r"(r2)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
+      : "memory");
+  return r0 | r1 | r2;
+}
+
 // try_wait with a suspend-time hint: the thread may sleep in the barrier until
 // the phase completes (or the hint expires) instead of spinning, leaving the
 // issue slots of its sub-partition to the warps that have work.
@@ -187,26 +206,27 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
+// D[tmem] (+)= A[smem desc] * B[smem desc].  No "memory" clobber: the MMA
+// touches no memory the compiler tracks (its operands are ordered by the
+// barrier waits, which are asm volatile too), and a clobber here would make
+// the issuing thread reload spilled values between MMAs.
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]
+// D[tmem] (+)= A[tmem] * B[smem desc]  (no "memory" clobber, as above)
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.

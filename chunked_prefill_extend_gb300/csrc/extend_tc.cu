@@ -86,16 +86,24 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int never;  // stays 0: the abort flag of the final drain waits, which must not give up early
 };
 
 __device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 96;"); }
 __device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 200;"); }
 
 // Work item: key tiles [kv_lo, kv_hi) of one unit.
+// The two query tiles' fields are kept as separate scalars and picked with a
+// select: indexing a two-element array with a runtime tile number would put the
+// array in local memory, whose loads share the L1/shared-memory path that the
+// tensor core's operand reads keep busy.
 struct Item {
   int seq, g, q0, E, P, kv_lo, kv_hi;
-  int i0[2], kv_end[2], n_kt[2];
+  int i0_0, i0_1, kv_end_0, kv_end_1, n_kt_0, n_kt_1;
   bool whole;
+  __device__ __forceinline__ int i0(int t) const { return t ? i0_1 : i0_0; }
+  __device__ __forceinline__ int kv_end(int t) const { return t ? kv_end_1 : kv_end_0; }
+  __device__ __forceinline__ int n_kt(int t) const { return t ? n_kt_1 : n_kt_0; }
 };
 
 // Fills `it` for work item i (part i / n_units of unit i % n_units); false if
@@ -114,12 +122,12 @@ __device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, int n_un
   it.q0 = a.qo_indptr[e.seq];
   it.E = a.qo_indptr[e.seq + 1] - it.q0;
   it.P = a.prefix_len[e.seq];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    it.i0[t] = (2 * e.pair + t) * a.tok;
-    it.kv_end[t] = it.i0[t] < it.E ? it.P + min(it.E, it.i0[t] + a.tok) : 0;
-    it.n_kt[t] = (it.kv_end[t] + kBlockN - 1) / kBlockN;
-  }
+  it.i0_0 = 2 * e.pair * a.tok;
+  it.i0_1 = it.i0_0 + a.tok;
+  it.kv_end_0 = it.i0_0 < it.E ? it.P + min(it.E, it.i0_0 + a.tok) : 0;
+  it.kv_end_1 = it.i0_1 < it.E ? it.P + min(it.E, it.i0_1 + a.tok) : 0;
+  it.n_kt_0 = (it.kv_end_0 + kBlockN - 1) / kBlockN;
+  it.n_kt_1 = (it.kv_end_1 + kBlockN - 1) / kBlockN;
   return true;
 }
 
@@ -161,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
+    bars->never = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -197,24 +206,26 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (is_k) {
           if (items > 0 &&
               !mbar_wait(&bars->q_empty, (items - 1) & 1, abort, a.wait_ns, a.status, kDetailQFull)) break;
-          const int n_q = it.n_kt[1] > 0 ? 2 : 1;
+          const int n_q = it.n_kt_1 > 0 ? 2 : 1;
           mbar_arrive_expect_tx(&bars->q_full, n_q * C::kTileBytes);
           for (int t = 0; t < n_q; ++t)
             for (int h = 0; h < C::kHalves; ++h)
               tma_load_3d(smem + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &a.tm_q, &bars->q_full, h * 64,
-                          it.g * a.group, it.q0 + it.i0[t]);
+                          it.g * a.group, it.q0 + it.i0(t));
           ++items;
         }
-        const int kv_max = max(it.kv_end[0], it.kv_end[1]);
+        const int kv_max = max(it.kv_end_0, it.kv_end_1);
         const int32_t* pt = a.page_table + static_cast<int64_t>(it.seq) * a.max_pages;
         for (int j = it.kv_lo; j < it.kv_hi; ++j, ++cnt) {
           const int st = cnt % ns;
           const int use = cnt / ns;
           const int keys = min(kBlockN, kv_max - j * kBlockN);
           const int npg = (keys + kPage - 1) / kPage;
-          int rows[kBlockN / kPage];
+          int rows[kBlockN / kPage];  // unrolled loops below keep it in registers
           bool contiguous = npg == kBlockN / kPage;  // eight pages back to back: one box per half
-          for (int pg = 0; pg < npg; ++pg) {
+#pragma unroll
+          for (int pg = 0; pg < kBlockN / kPage; ++pg) {
+            if (pg >= npg) break;
             const int pid = pt[j * (kBlockN / kPage) + pg];
             if (pid < 0 || pid >= a.num_pages) {
               record_error(a.status, kStatusDeviceArg, kDetailBadPage);
@@ -235,19 +246,22 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             for (int h = 0; h < C::kHalves; ++h)
               tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes, tm128, &full[st], h * 64, it.g, rows[0]);
           } else {
-            for (int pg = 0; pg < npg; ++pg)
+#pragma unroll
+            for (int pg = 0; pg < kBlockN / kPage; ++pg) {
+              if (pg >= npg) break;
               for (int h = 0; h < C::kHalves; ++h)
                 tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64,
                             it.g, rows[pg]);
+            }
           }
         }
       }
       // Drain: every copy issued must land before the CTA exits.
       if (*abort) {
-        volatile int no_abort = 0;
-        if (is_k && items > 0) mbar_wait(&bars->q_full, (items - 1) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+        volatile int* no_abort = &bars->never;
+        if (is_k && items > 0) mbar_wait(&bars->q_full, (items - 1) & 1, no_abort, kDrainNs, a.status, kDetailDrain);
         for (int n = max(0, cnt - ns); n < cnt; ++n)
-          mbar_wait(&full[n % ns], (n / ns) & 1, &no_abort, kDrainNs, a.status, kDetailDrain);
+          mbar_wait(&full[n % ns], (n / ns) & 1, no_abort, kDrainNs, a.status, kDetailDrain);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -264,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_commit(&bars->s_full[t]);
       };
       int kc = 0, vc = 0, items = 0;
-      int pc[2] = {0, 0};
+      int pc0 = 0, pc1 = 0;  // P hand-offs consumed per tile
       bool ok = true;
       Item it;
       for (int wi = cta; ok && wi < n_items; wi += nc) {
@@ -276,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
         ++items;
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (it.kv_lo < it.n_kt[t]) issue_s(t, kc % NK);
+        if (it.kv_lo < it.n_kt_0) issue_s(0, kc % NK);
+        if (it.kv_lo < it.n_kt_1) issue_s(1, kc % NK);
         tc_commit(&bars->k_empty[kc % NK]);
         ++kc;
         for (int j = it.kv_lo; j < it.kv_hi; ++j) {
@@ -285,24 +299,35 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           // the MMA bursts below are separated only by the softmax hand-offs.
           const int sv_st = vc % NV;
           const bool more = j + 1 < it.kv_hi;
-          if (!mbar_wait(&bars->v_full[sv_st], (vc / NV) & 1, abort, a.wait_ns, a.status, kDetailVFull) ||
-              (more && !mbar_wait(&bars->k_full[kc % NK], (kc / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull))) {
+          // V_j, K_{j+1} and tile 0's P are usually ready: test all three at
+          // once and wait only for what is not.
+          const bool need_p0 = j < it.n_kt_0;
+          const uint32_t ready =
+              mbar_test3(&bars->v_full[sv_st], (vc / NV) & 1, &bars->k_full[kc % NK], (kc / NK) & 1,
+                         &bars->p_full[0], pc0 & 1);
+          if ((!(ready & 1u) &&
+               !mbar_wait(&bars->v_full[sv_st], (vc / NV) & 1, abort, a.wait_ns, a.status, kDetailVFull)) ||
+              (more && !(ready & 2u) &&
+               !mbar_wait(&bars->k_full[kc % NK], (kc / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull))) {
             ok = false;
             break;
           }
+          const bool p0_ready = need_p0 && (ready & 4u);
           const uint64_t vdesc =
               smem_desc_sw128(smem_u32(smem + C::kVOff + sv_st * C::kTileBytes), C::kHalfBytes, 1024);
-          for (int t = 0; t < 2; ++t) {
-            if (j >= it.n_kt[t]) continue;
-            if (!mbar_wait(&bars->p_full[t], pc[t] & 1, abort, a.wait_ns, a.status, kDetailPFull)) {
-              ok = false;
-              break;
-            }
-            ++pc[t];
+          // PV of tile t, then the next S of tile t; called with literal tile
+          // numbers so every per-tile value resolves at compile time.
+          auto tile_step = [&](const int t) -> bool {
+            if (j >= it.n_kt(t)) return true;
+            int& pct = t ? pc1 : pc0;
+            if (!(t == 0 && p0_ready) &&
+                !mbar_wait(&bars->p_full[t], pct & 1, abort, a.wait_ns, a.status, kDetailPFull))
+              return false;
+            ++pct;
             tc_fence_after();
             const uint32_t dcol = tmem + 256 + t * D;
             const uint32_t acol = tmem + t * 128;
-            const int keys = min(kBlockN, it.kv_end[t] - j * kBlockN);
+            const int keys = min(kBlockN, it.kv_end(t) - j * kBlockN);
             const uint32_t first = j > it.kv_lo ? 1u : 0u;
             if (keys == kBlockN) {
 #pragma unroll
@@ -315,12 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
                 tc_mma_ts(dcol, acol + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 / 16)), idesc_pv,
                           (first || kk > 0) ? 1u : 0u);
             }
-            if (j + 1 < min(it.kv_hi, it.n_kt[t]))
+            if (j + 1 < min(it.kv_hi, it.n_kt(t)))
               issue_s(t, kc % NK);
             else
               tc_commit(&bars->o_done[t]);
+            return true;
+          };
+          if (!tile_step(0) || !tile_step(1)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
           tc_commit(&bars->v_empty[sv_st]);
           ++vc;
           if (more) {
@@ -332,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       }
       // Drain: wait until every MMA issued above has completed.
       tc_commit(&bars->drain);
-      volatile int no_abort = 0;
-      mbar_wait(&bars->drain, 0, &no_abort, kDrainNs, a.status, kDetailDrain);
+      mbar_wait(&bars->drain, 0, &bars->never, kDrainNs, a.status, kDetailDrain);
     }
   } else {
     setmaxnreg_inc_softmax();
@@ -351,9 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     Item it;
     for (int wi = cta; ok && wi < n_items; wi += nc) {
       if (!load_item(a, wi, n_units, parts, it)) continue;
-      const int i = it.i0[t] + r / a.group;       // token index within the chunk
+      const int i0t = it.i0(t);
+      const int i = i0t + r / a.group;              // token index within the chunk
       const int lim = it.P + min(i, it.E - 1);    // last key this row may see
-      const int jhi = min(it.kv_hi, it.n_kt[t]);
+      const int jhi = min(it.kv_hi, it.n_kt(t));
       const int R = t * kBlockM + r;               // row of the unit
       float* part = a.sched.partial + static_cast<size_t>(wi) * slot_floats;
       if (it.kv_lo >= jhi) {
@@ -393,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           sv[96 + x] = __uint_as_float(r3[x]);
         }
         const int kb = j * kBlockN;
-        if (kb + kBlockN - 1 > it.P + it.i0[t]) {  // tile crosses the diagonal or the end: mask
+        if (kb + kBlockN - 1 > it.P + i0t) {  // tile crosses the diagonal or the end: mask
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             if (kb + c > lim) sv[c] = -INFINITY;
