@@ -117,3 +117,61 @@ def plan_mixed_step(token_budget: int, decode_ctx_len: list[int], prefill_prefix
         qo.append(qo[-1] + extend)
     return {"qo_indptr": qo, "prefix_len": prefix, "kv_len": kv, "n_decode": n_dec,
             "extend_len": extend}
+
+
+def plan_schedule(token_budget: int, running: list[tuple[int, int]],
+                  waiting: list[tuple[int, int]]) -> dict:
+    """One scheduling step over running and waiting requests, as the vLLM
+    tutorial's section 5 sketches ``schedule()`` (memory allocation and
+    preemption left out: the caller owns the cache).
+
+    running: (computed, need) per running request, in queue order: tokens whose
+        K/V are already cached and tokens still to process (1 for a decode, the
+        unfinished part of a prompt for a prefill continuation).
+    waiting: (cached, prompt) per waiting request, in queue order: prefix-cache
+        hit and prompt length; such a request needs prompt - cached tokens.
+
+    Running requests take min(need, budget left) in order until the budget is
+    spent; then waiting requests are admitted in order the same way while any
+    budget is left.  The granted token count is the chunk: a prompt that does
+    not fit is cut, and the rest waits for the next step.
+
+    The batch lists every scheduled request as one sequence: those granted a
+    single token first (decode rows, in scheduling order), then the others in
+    scheduling order.  prefix_len is the request's cached tokens, kv_len adds
+    the granted ones; seq_request names the request (running index r, or
+    len(running) + waiting index).
+    """
+    if token_budget <= 0:
+        raise ValueError("token_budget must be > 0")
+    for computed, need in running:
+        if computed < 0 or need < 1:
+            raise ValueError("a running request needs computed >= 0 and need >= 1")
+    for cached, prompt in waiting:
+        if cached < 0 or prompt - cached < 1:
+            raise ValueError("a waiting request needs cached >= 0 and prompt - cached >= 1")
+    left = token_budget
+    granted = []
+    for computed, need in running:
+        take = min(need, left)
+        granted.append(take)
+        left -= take
+    admitted = 0
+    for cached, prompt in waiting:
+        if left == 0:
+            granted.append(0)
+            continue
+        take = min(prompt - cached, left)
+        granted.append(take)
+        left -= take
+        admitted += 1
+    base = [c for c, _ in running] + [c for c, _ in waiting]
+    order = ([r for r, g in enumerate(granted) if g == 1] +
+             [r for r, g in enumerate(granted) if g > 1])
+    qo = [0]
+    for r in order:
+        qo.append(qo[-1] + granted[r])
+    return {"granted": granted, "n_admitted": admitted, "qo_indptr": qo,
+            "prefix_len": [base[r] for r in order],
+            "kv_len": [base[r] + granted[r] for r in order],
+            "seq_request": order, "n_decode": sum(1 for g in granted if g == 1)}

@@ -98,3 +98,91 @@ def test_mixed_step_edges():
     assert out["qo_indptr"] == [0, 64] and out["prefix_len"] == [0]
     with pytest.raises(ValueError):
         plan.plan_mixed_step(0, [5], 0, 10)
+
+
+@pytest.mark.parametrize("case", GOLDEN["schedule_examples"], ids=lambda c: str(c["budget"]))
+def test_schedule_matches_pages(case):
+    out = plan.plan_schedule(case["budget"], [tuple(x) for x in case["running"]],
+                             [tuple(x) for x in case["waiting"]])
+    assert out["granted"] == case["granted"]
+    assert out["n_admitted"] == case["n_admitted"]
+    reqs = [tuple(x) for x in case["running"]] + [(c, p - c) for c, p in case["waiting"]]
+    # one-token sequences first, then the chunks, each in scheduling order
+    ones = [r for r, g in enumerate(case["granted"]) if g == 1]
+    many = [r for r, g in enumerate(case["granted"]) if g > 1]
+    assert out["seq_request"] == ones + many
+    assert out["prefix_len"] == [reqs[r][0] for r in ones + many]
+    assert out["kv_len"] == [reqs[r][0] + case["granted"][r] for r in ones + many]
+    assert out["qo_indptr"][-1] == sum(case["granted"])
+    if "next_step_running" in case:  # the cut prompt continues from where it stopped
+        (cached, prompt), = case["waiting"]
+        nxt = [(cached + case["granted"][0], prompt - cached - case["granted"][0])]
+        assert nxt == [tuple(x) for x in case["next_step_running"]]
+
+
+def test_schedule_waiting_need_excludes_prefix_cache_hit():
+    """A waiting request needs its prompt minus the cached prefix, and its
+    chunk starts after that prefix (the sketch's num_tokens - num_cached)."""
+    out = plan.plan_schedule(2048, [], [(1000, 1500), (256, 4096)])
+    assert out["granted"] == [500, 1548]
+    assert out["prefix_len"] == [1000, 256] and out["kv_len"] == [1500, 1804]
+
+
+def test_schedule_reproduces_chunk_plan():
+    """One request scheduled step after step under a fixed budget is cut exactly
+    as the chunk planner cuts it (same query and prefix lengths)."""
+    for n, hit, c in [(4000, 0.0, 512), (10000, 0.0, 4096), (32768, 0.5, 8192), (999, 0.3, 128)]:
+        cached, eff = plan.effective_input_length(n, hit)
+        steps = []
+        out = plan.plan_schedule(c, [], [(cached, n)])
+        while True:
+            steps.append((out["prefix_len"][0], out["qo_indptr"][-1]))
+            done = out["kv_len"][0]
+            if done == n:
+                break
+            out = plan.plan_schedule(c, [(done, n - done)], [])
+        assert steps == [(ch.prefix_len, ch.query_len) for ch in plan.plan_chunks(n, hit, c)]
+
+
+def test_schedule_reduces_to_mixed_step():
+    """Decode rows plus one running prefill: the same batch as the mixed-step planner."""
+    for budget, ctx, P, rem in [(2304, list(range(600, 856)), 30720, 10000), (64, [5, 6], 100, 0),
+                                (3, [5, 6, 7, 8], 100, 50), (64, [], 0, 1000), (300, [9] * 10, 4096, 100)]:
+        running = [(L - 1, 1) for L in ctx] + ([(P, rem)] if rem > 0 else [])
+        a = plan.plan_schedule(budget, running, [])
+        b = plan.plan_mixed_step(budget, ctx, P, rem)
+        assert a["qo_indptr"] == b["qo_indptr"] and a["prefix_len"] == b["prefix_len"]
+        assert a["kv_len"] == b["kv_len"]
+        if b["extend_len"] != 1:
+            assert a["n_decode"] == b["n_decode"]
+
+
+def test_schedule_invariants():
+    import random
+    rng = random.Random(7)
+    for _ in range(300):
+        budget = rng.randint(1, 5000)
+        running = [(rng.randint(0, 9000), rng.choice([1, 1, 1, rng.randint(1, 3000)])) for _ in range(rng.randint(0, 12))]
+        waiting = []
+        for _ in range(rng.randint(0, 6)):
+            cached = rng.randint(0, 2000)
+            waiting.append((cached, cached + rng.randint(1, 3000)))
+        out = plan.plan_schedule(budget, running, waiting)
+        g = out["granted"]
+        needs = [nd for _, nd in running] + [p - c for c, p in waiting]
+        assert sum(g) <= budget and all(0 <= x <= nd for x, nd in zip(g, needs))
+        # a request cut short (or skipped) means the budget ran out at it
+        for r, (x, nd) in enumerate(zip(g, needs)):
+            if x < nd:
+                assert sum(g[:r + 1]) == budget and all(y == 0 for y in g[r + 1:])
+        # admitted waiting requests are a prefix of the queue
+        gw = g[len(running):]
+        assert out["n_admitted"] == sum(1 for x in gw if x > 0) and all(x > 0 for x in gw[:out["n_admitted"]])
+        assert out["qo_indptr"][-1] == sum(g) and out["n_decode"] == sum(1 for x in g if x == 1)
+
+
+def test_schedule_argument_errors():
+    for args in [(0, [], [(0, 10)]), (10, [(-1, 1)], []), (10, [(5, 0)], []), (10, [], [(10, 10)]),
+                 (10, [], [(-1, 5)])]:
+        with pytest.raises(ValueError):
+            plan.plan_schedule(*args)
