@@ -25,7 +25,7 @@ CPE_OK, CPE_ERR_INVALID_ARG, CPE_ERR_UNSUPPORTED, CPE_ERR_CAPACITY, CPE_ERR_CUDA
     CPE_ERR_DEVICE_ARG = range(7)
 CPE_F32, CPE_BF16 = 0, 1
 
-EXPORTS = ["cpe_plan_chunks", "cpe_plan_budget", "cpe_plan_mixed_step", "cpe_kv_append",
+EXPORTS = ["cpe_plan_chunks", "cpe_plan_budget", "cpe_plan_mixed_step", "cpe_plan_schedule", "cpe_kv_append",
            "cpe_workspace_size", "cpe_extend_attention", "cpe_mixed_step", "cpe_decode_attention",
            "cpe_get_device_status", "cpe_set_wait_limit_ns", "cpe_status_string", "cpe_last_error",
            "cpe_launch_count", "cpe_decode_attention_noalloc"]
@@ -44,6 +44,8 @@ _lib.cpe_plan_chunks.argtypes = [_i64, _f64, _i32, _i32, ctypes.POINTER(_Chunk),
 _lib.cpe_plan_budget.argtypes = [_i32, _i32, _vp, _vp, ctypes.POINTER(_i32)]
 _lib.cpe_plan_mixed_step.argtypes = [_i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, ctypes.POINTER(_i32),
                                      ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
+_lib.cpe_plan_schedule.argtypes = [_i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, ctypes.POINTER(_i32), _vp, _vp, _vp,
+                                   _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
 _lib.cpe_kv_append.argtypes = [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                _i32, ctypes.c_int, _vp]
 _lib.cpe_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
@@ -140,6 +142,25 @@ def cpe_plan_mixed_step(token_budget: int, decode_ctx_len, prefill_prefix_len: i
     k = ns.value
     return {"qo_indptr": list(qo[:k + 1]), "prefix_len": list(pl[:k]), "kv_len": list(kv[:k]),
             "n_decode": nd.value, "extend_len": ext.value}
+
+
+def cpe_plan_schedule(token_budget: int, running, waiting):
+    """running: [(computed, need)], waiting: [(cached, prompt)], both in queue order."""
+    nr, nw = len(running), len(waiting)
+    n = nr + nw
+    rc = (_i32 * max(1, nr))(*[c for c, _ in running])
+    rn = (_i32 * max(1, nr))(*[x for _, x in running])
+    wc = (_i32 * max(1, nw))(*[c for c, _ in waiting])
+    wp = (_i32 * max(1, nw))(*[p for _, p in waiting])
+    granted = (_i32 * max(1, n))()
+    qo = (_i32 * (n + 1))()
+    pl, kv, sr = (_i32 * max(1, n))(), (_i32 * max(1, n))(), (_i32 * max(1, n))()
+    adm, ns, nd = _i32(0), _i32(0), _i32(0)
+    _check(_lib.cpe_plan_schedule(token_budget, nr, rc, rn, nw, wc, wp, granted, ctypes.byref(adm), qo, pl, kv, sr,
+                                  ctypes.byref(ns), ctypes.byref(nd)), "cpe_plan_schedule")
+    k = ns.value
+    return {"granted": list(granted[:n]), "n_admitted": adm.value, "qo_indptr": list(qo[:k + 1]),
+            "prefix_len": list(pl[:k]), "kv_len": list(kv[:k]), "seq_request": list(sr[:k]), "n_decode": nd.value}
 
 
 def cpe_workspace_size(n_seqs: int, total_q: int, h_q: int, h_kv: int, d: int, max_kv_len: int) -> int:

@@ -137,3 +137,61 @@ extern "C" cpe_status cpe_plan_mixed_step(int32_t token_budget, int32_t n_decode
   *n_seqs = ns;
   return CPE_OK;
 }
+
+extern "C" cpe_status cpe_plan_schedule(int32_t token_budget, int32_t n_running, const int32_t* running_computed,
+                                        const int32_t* running_need, int32_t n_waiting,
+                                        const int32_t* waiting_cached, const int32_t* waiting_prompt,
+                                        int32_t* granted, int32_t* n_admitted, int32_t* qo_indptr,
+                                        int32_t* prefix_len, int32_t* kv_len, int32_t* seq_request,
+                                        int32_t* n_seqs, int32_t* n_decode) {
+  const char* fn = "cpe_plan_schedule";
+  auto bad = [&](const char* why) {
+    cpe::set_last_error(std::string(fn) + ": " + why);
+    return CPE_ERR_INVALID_ARG;
+  };
+  if (token_budget <= 0) return bad("token_budget must be > 0");
+  if (n_running < 0 || n_waiting < 0 || static_cast<int64_t>(n_running) + n_waiting > INT32_MAX - 1)
+    return bad("request counts must be >= 0");
+  if ((n_running > 0 && (!running_computed || !running_need)) ||
+      (n_waiting > 0 && (!waiting_cached || !waiting_prompt)))
+    return bad("null request arrays");
+  const int32_t n = n_running + n_waiting;
+  if (!n_admitted || !qo_indptr || !n_seqs || !n_decode ||
+      (n > 0 && (!granted || !prefix_len || !kv_len || !seq_request)))
+    return bad("null output arrays");
+  for (int32_t r = 0; r < n_running; ++r) {
+    if (running_computed[r] < 0 || running_need[r] < 1) return bad("a running request needs computed >= 0, need >= 1");
+    if (static_cast<int64_t>(running_computed[r]) + running_need[r] > INT32_MAX) return bad("length overflows int32");
+  }
+  for (int32_t w = 0; w < n_waiting; ++w)
+    if (waiting_cached[w] < 0 || static_cast<int64_t>(waiting_prompt[w]) - waiting_cached[w] < 1)
+      return bad("a waiting request needs cached >= 0 and prompt - cached >= 1");
+  // grants: running requests in order, then waiting ones while budget is left
+  int32_t left = token_budget;
+  int32_t admitted = 0;
+  for (int32_t k = 0; k < n; ++k) {
+    const int32_t need = k < n_running ? running_need[k] : waiting_prompt[k - n_running] - waiting_cached[k - n_running];
+    const int32_t take = need < left ? need : left;
+    granted[k] = take;
+    left -= take;
+    if (k >= n_running && take > 0) ++admitted;
+  }
+  // the batch: one-token sequences first, then the chunks, each in scheduling order
+  int32_t ns = 0, nd = 0;
+  qo_indptr[0] = 0;
+  for (int pass = 0; pass < 2; ++pass)
+    for (int32_t k = 0; k < n; ++k) {
+      if (granted[k] == 0 || (pass == 0) != (granted[k] == 1)) continue;
+      const int32_t base = k < n_running ? running_computed[k] : waiting_cached[k - n_running];
+      prefix_len[ns] = base;
+      kv_len[ns] = base + granted[k];
+      seq_request[ns] = k;
+      qo_indptr[ns + 1] = qo_indptr[ns] + granted[k];
+      ++ns;
+      if (pass == 0) ++nd;
+    }
+  *n_admitted = admitted;
+  *n_seqs = ns;
+  *n_decode = nd;
+  return CPE_OK;
+}

@@ -137,6 +137,39 @@ cpe_status cpe_plan_mixed_step(int32_t token_budget, int32_t n_decode,
                                int32_t* extend_len_out);
 
 /*
+ * cpe_plan_schedule — one scheduling step over running and waiting requests
+ * under one token budget, laid out as the varlen batch cpe_mixed_step takes
+ * (host only).
+ *   vLLM tutorial, section 5 (the schedule() sketch and its worked example):
+ *   running requests, in order, each take min(need, budget left); then waiting
+ *   requests, in order, are admitted the same way while budget is left.  A
+ *   prompt that does not fit is cut there: the granted count is its chunk.
+ *   Memory allocation and preemption are the caller's and are not modelled.
+ * running_computed[n_running], running_need[n_running] (host): tokens whose
+ *   K/V are already cached, and tokens still to process (>= 1; 1 for a decode,
+ *   the unfinished part of the prompt for a prefill continuation).
+ * waiting_cached[n_waiting], waiting_prompt[n_waiting] (host): prefix-cache hit
+ *   and prompt length; a waiting request needs prompt - cached >= 1 tokens.
+ * Outputs (host, caller-owned; let n = n_running + n_waiting):
+ *   granted[n]: tokens granted per request (running first, then waiting);
+ *   *n_admitted: waiting requests granted any tokens (a prefix of the queue);
+ *   the batch, one sequence per request granted tokens: those granted exactly
+ *   one token first (decode rows; sequences 0 .. *n_decode-1, in scheduling
+ *   order), then the others in scheduling order:
+ *   qo_indptr[n + 1], prefix_len[n] (= the request's cached tokens),
+ *   kv_len[n] (= prefix_len + granted), seq_request[n] (the request's index:
+ *   r for running r, n_running + w for waiting w), *n_seqs, *n_decode.
+ * Errors: CPE_ERR_INVALID_ARG for token_budget <= 0, negative counts, null
+ * arrays, computed < 0, need < 1, cached < 0, prompt - cached < 1, or a
+ * length that overflows int32.  Nothing is written on error.
+ */
+cpe_status cpe_plan_schedule(int32_t token_budget, int32_t n_running, const int32_t* running_computed,
+                             const int32_t* running_need, int32_t n_waiting, const int32_t* waiting_cached,
+                             const int32_t* waiting_prompt, int32_t* granted, int32_t* n_admitted,
+                             int32_t* qo_indptr, int32_t* prefix_len, int32_t* kv_len, int32_t* seq_request,
+                             int32_t* n_seqs, int32_t* n_decode);
+
+/*
  * cpe_kv_append — write the round's new K/V rows into the paged caches.
  *   SGLang article, implementation section (the request's req_to_token row
  *   keeps its page slots across chunks); mini-infer article, write_prefill_kv.

@@ -18,7 +18,7 @@ import subprocess
 import numpy as np
 import torch
 
-from .plan import Chunk, budget_truncate, effective_input_length, plan_chunks, plan_mixed_step
+from .plan import Chunk, budget_truncate, effective_input_length, plan_chunks, plan_mixed_step, plan_schedule
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "cpe_oracle.c")
@@ -27,7 +27,7 @@ _lib = None
 
 F32, BF16 = 0, 1
 
-__all__ = ["Chunk", "budget_truncate", "effective_input_length", "plan_chunks", "plan_mixed_step",
+__all__ = ["Chunk", "budget_truncate", "effective_input_length", "plan_chunks", "plan_mixed_step", "plan_schedule",
            "build", "extend_attention", "extend_attention_two_stage", "causal_attention",
            "kv_append", "num_threads", "set_fault"]
 

@@ -1,6 +1,7 @@
 """The C-ABI library loads, exports what include/cpe.h declares, validates
 arguments on the host, and its planners match the oracle's bit for bit.
 No CUDA call is made here (host-only entry points and pre-launch checks)."""
+import json
 import os
 import random
 import re
@@ -73,6 +74,30 @@ def test_plan_budget_and_mixed_step_match_oracle():
         a = cpe.cpe_plan_mixed_step(budget, ctx, P, rem)
         b = oracle.plan_mixed_step(budget, ctx, P, rem)
         assert a == b
+
+
+def test_plan_schedule_matches_oracle():
+    rng = random.Random(12)
+    for _ in range(300):
+        budget = rng.randint(1, 6000)
+        running = [(rng.randint(0, 40000), rng.choice([1, 1, rng.randint(1, 4000)])) for _ in range(rng.randint(0, 40))]
+        waiting = []
+        for _ in range(rng.randint(0, 8)):
+            cached = rng.randint(0, 5000)
+            waiting.append((cached, cached + rng.randint(1, 6000)))
+        assert cpe.cpe_plan_schedule(budget, running, waiting) == oracle.plan_schedule(budget, running, waiting)
+    golden = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "plan_vectors.json")))
+    for case in golden["schedule_examples"]:
+        out = cpe.cpe_plan_schedule(case["budget"], [tuple(x) for x in case["running"]],
+                                    [tuple(x) for x in case["waiting"]])
+        assert out["granted"] == case["granted"] and out["n_admitted"] == case["n_admitted"]
+
+
+def test_plan_schedule_errors():
+    for budget, running, waiting in [(0, [], [(0, 5)]), (8, [(-1, 2)], []), (8, [(3, 0)], []), (8, [], [(5, 5)]),
+                                     (8, [], [(-2, 5)]), (8, [(2**31 - 10, 20)], [])]:
+        with pytest.raises(cpe.CpeError):
+            cpe.cpe_plan_schedule(budget, running, waiting)
 
 
 def test_mixed_step_cfg4_shape():

@@ -259,6 +259,50 @@ def test_cfg4_mixed_sampled(cpe):
     np.testing.assert_allclose(lse[256:][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 
+def _scheduled_step(cpe, seed, budget, running, waiting):
+    """One step laid out by the scheduling planner and run through cpe_mixed_step."""
+    plan = cpe.cpe_plan_schedule(budget, running, waiting)
+    lens = [(p, plan["qo_indptr"][i + 1] - plan["qo_indptr"][i]) for i, p in enumerate(plan["prefix_len"])]
+    b = varlen_batch(seed, lens, 32, 8, 128)
+    lse = torch.empty(b["q"].shape[0], 32, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(b["q"], b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"],
+                                i32(b["qo"]), i32(b["pl"]), plan["n_decode"], b["max_kv"], lse=lse)
+    _status_ok(cpe)
+    return plan, b, out, lse
+
+
+def test_scheduled_step_several_prefills_full(cpe):
+    """Decode rows, a running prefill continuation and a waiting request with a
+    prefix-cache hit cut to its first chunk, in one step; every row checked."""
+    running = [(37, 1), (2048, 1), (5, 1), (999, 1), (900, 300), (0, 1)]
+    waiting = [(200, 500), (0, 64)]
+    plan, b, out, lse = _scheduled_step(cpe, 70, 512, running, waiting)
+    assert plan["granted"] == [1, 1, 1, 1, 300, 1, 207, 0] and plan["n_decode"] == 5
+    kc, vc = b["k_cache"].cpu().clone(), b["v_cache"].cpu().clone()
+    ref_o, ref_l = oracle.extend_attention(b["q"].cpu(), kc, vc, b["page_table_host"], b["qo"], b["pl"], 32, 8)
+    check_close(out, ref_o, "scheduled step")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
+def test_scheduled_step_pages_example_sampled(cpe):
+    """The vLLM tutorial's step at its own sizes: 8 decodes, R's remaining 1440
+    tokens, W1 cut to 600 (GQA 32/8, d=128); decode rows in full, chunk rows
+    sampled."""
+    running = [(600 + 97 * k, 1) for k in range(8)] + [(3000, 1440)]
+    waiting = [(0, 900), (0, 700)]
+    plan, b, out, lse = _scheduled_step(cpe, 71, 2048, running, waiting)
+    assert plan["granted"][8:] == [1440, 600, 0] and plan["qo_indptr"][-1] == 2048
+    qo = plan["qo_indptr"]
+    for s in range(len(plan["prefix_len"])):
+        E = qo[s + 1] - qo[s]
+        rows = list(range(E)) if E <= 8 else W.sample_rows(E, 32, 48, 500 + s)
+        kc, vc, pt = extract_pages(b["k_cache"], b["v_cache"], b["page_table_host"], [s], [plan["kv_len"][s]])
+        q = b["q"][qo[s]:qo[s + 1]].cpu()
+        ref_o, ref_l = oracle.extend_attention(q, kc, vc, pt, [0, E], [plan["prefix_len"][s]], 32, 8, rows=rows)
+        check_close(out[qo[s]:qo[s + 1]][rows], ref_o, f"sequence {s}")
+        np.testing.assert_allclose(lse[qo[s]:qo[s + 1]][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
 # ---------------------------------------------------------------- device-side errors
 
 def test_bad_page_id_is_reported(cpe):
