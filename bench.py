@@ -268,8 +268,91 @@ class Mixed:
         return flops, dt, f"{len(picks)} decode rows x {spec.h_q} heads (all keys)"
 
 
+class Scheduled(Mixed):
+    """One scheduling step over running and waiting requests: the budget-laid
+    varlen batch (decode rows, several prefill chunks) through cpe_mixed_step."""
+
+    def __init__(self, spec, device, cpe):
+        self.spec, self.cpe, self.device = spec, cpe, device
+        self.running, self.waiting = W.scheduled_requests(spec)
+        self.plan = cpe.cpe_plan_schedule(spec.token_budget, self.running, self.waiting)
+        qo = self.plan["qo_indptr"]
+        lens = [(p, qo[i + 1] - qo[i]) for i, p in enumerate(self.plan["prefix_len"])]
+        self.mb = W.make_scheduled(spec, lens, device=device)
+        self.qo = torch.tensor(qo, dtype=torch.int32, device=device)
+        self.pl = torch.tensor(self.plan["prefix_len"], dtype=torch.int32, device=device)
+        self.max_kv = max(self.plan["kv_len"])
+        nd = self.plan["n_decode"]
+        self.ws = cpe.alloc_workspace(len(lens), self.mb.q.shape[0], spec.h_q, spec.h_kv, spec.d, self.max_kv,
+                                      device)
+        self.out = torch.empty_like(self.mb.q)
+        dec_L = self.plan["kv_len"][:nd]
+        self.extend_flops = sum(chunk_flops(spec.d, spec.h_q, P, E) for P, E in lens[nd:])
+        self.flops = self.extend_flops + sum(4.0 * spec.d * spec.h_q * L for L in dec_L)
+        self.decode_bytes = sum(2.0 * L * spec.h_kv * spec.d * 2 + 2.0 * spec.h_q * spec.d * 2 for L in dec_L)
+        self.tokens = qo[-1]
+        self.in_bytes = sum(t.numel() * t.element_size() for t in (self.mb.q, self.mb.k_new, self.mb.v_new))
+        # the chunks alone, for the extend call's roofline
+        r0 = qo[nd]
+        self.q_ext = self.mb.q[r0:]
+        self.out_ext = self.out[r0:]
+        self.qo_ext = torch.tensor([x - r0 for x in qo[nd:]], dtype=torch.int32, device=device)
+        self.pl_ext = self.pl[nd:]
+        self.pt_ext = self.mb.page_table[nd:]
+        self.lens = lens
+        self.kernel = "extend_tc_kernel"
+        self.bound = "tensor"
+        self.small = False
+
+    def step(self, ev=None, q=None, k=None, v=None, out=None):
+        cpe, mb, spec = self.cpe, self.mb, self.spec
+        q = mb.q if q is None else q
+        k = mb.k_new if k is None else k
+        v = mb.v_new if v is None else v
+        out = self.out if out is None else out
+        cpe.cpe_plan_schedule(spec.token_budget, self.running, self.waiting)
+        cpe.cpe_mixed_step(q, k, v, mb.k_cache, mb.v_cache, mb.page_table, self.qo, self.pl, self.plan["n_decode"],
+                           self.max_kv, out=out, workspace=self.ws)
+        return out
+
+    def extend_only(self, ev):
+        """The prefill chunks alone through cpe_extend_attention (the tensor roofline)."""
+        ev[0].append(torch.cuda.Event(enable_timing=True))
+        ev[0][-1].record()
+        self.cpe.cpe_extend_attention(self.q_ext, self.mb.k_cache, self.mb.v_cache, self.pt_ext, self.qo_ext,
+                                      self.pl_ext, self.max_kv, out=self.out_ext, workspace=self.ws)
+        ev[1].append(torch.cuda.Event(enable_timing=True))
+        ev[1][-1].record()
+
+    def oracle_sample(self, oracle, budget_s):
+        spec, mb, plan = self.spec, self.mb, self.plan
+        nd = plan["n_decode"]
+        qo = plan["qo_indptr"]
+        # four decode rows and two rows of every chunk, all heads, all keys
+        picks = list(range(0, nd, max(1, nd // 4)))[:4]
+        pg = mb.k_cache.shape[1]
+        flops, dt = 0.0, 0.0
+        for s in picks + list(range(nd, len(self.lens))):
+            E = qo[s + 1] - qo[s]
+            rows = [0] if E == 1 else [E // 3, E - 1]
+            L = plan["kv_len"][s]
+            n = -(-L // pg)
+            ids = mb.page_table_host[s, :n].long().to(mb.k_cache.device)
+            kc, vc = mb.k_cache[ids].cpu(), mb.v_cache[ids].cpu()
+            pt = torch.arange(n, dtype=torch.int32).view(1, -1)
+            q = mb.q[qo[s]:qo[s + 1]].cpu()
+            t0 = time.perf_counter()
+            oracle.extend_attention(q, kc, vc, pt, [0, E], [plan["prefix_len"][s]], spec.h_q, spec.h_kv, rows=rows)
+            dt += time.perf_counter() - t0
+            flops += sum(4.0 * spec.d * spec.h_q * (plan["prefix_len"][s] + r + 1) for r in rows)
+        return flops, dt, f"{len(picks)} decode rows and 2 rows of each of {len(self.lens) - nd} chunks x {spec.h_q} " \
+                          "heads (all keys of each row)"
+
+
 def make_workload(args, device, cpe):
     spec = W.CONFIGS[args.workload]
+    if isinstance(spec, W.ScheduledSpec):
+        return Scheduled(spec, device, cpe)
     if isinstance(spec, W.MixedSpec):
         if args.decode_rows:
             spec = W.shrink(spec, n_decode=args.decode_rows)
@@ -409,7 +492,23 @@ def run_ours(args, ws, rank, local):
     value = wl.flops * ws / (ms_per_step * 1e-3) / 1e12
 
     # dominant kernel, timed live with events on the launching stream
-    if isinstance(wl, Mixed):
+    if isinstance(wl, Scheduled):
+        ext_ev, dev_ev = ([], []), ([], [])
+        for _ in range(max(3, args.steps // 2)):
+            wl.extend_only(ext_ev)
+            wl.decode_only(dev_ev)
+        torch.cuda.synchronize()
+        kms = statistics.mean(a.elapsed_time(b) for a, b in zip(*ext_ev))
+        dms = statistics.mean(a.elapsed_time(b) for a, b in zip(*dev_ev))
+        achieved = wl.extend_flops / (kms * 1e-3) / 1e12
+        pk = peaks["bf16_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "traffic": None, "kernel": "extend attention call on the step's prefill chunks",
+                "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": wl.extend_flops,
+                "decode_rows": {"achieved": wl.decode_bytes / (dms * 1e-3) / 1e9, "unit": "GB/s",
+                                "peak": peaks["hbm_gbs"], "ms": dms},
+                "per_chunk": [{"prefix_len": P, "query_len": E} for P, E in wl.lens[wl.plan["n_decode"]:]]}
+    elif isinstance(wl, Mixed):
         dev_ev = ([], [])
         for _ in range(max(3, args.steps // 2)):
             wl.decode_only(dev_ev)
@@ -516,7 +615,7 @@ def run_reference(args, ws, rank, local):
     oracle.build()
     spec = W.CONFIGS[args.workload]
     # inputs generated on the CPU with the same seeded recipe (no GPU needed)
-    if isinstance(spec, W.MixedSpec):
+    if isinstance(spec, (W.MixedSpec, W.ScheduledSpec)):
         wl = _ref_mixed(spec)
     else:
         wl = _ref_chunked(spec)

@@ -86,14 +86,15 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t header_off, units_off, partial_off, part_o_off, part_ml_off, total;
+  size_t header_off, units_off, items_off, partial_off, part_o_off, part_ml_off, total;
   int unit_capacity, max_splits, slots;
 };
 
 int group_of(int h_q, int h_kv) { return h_q / h_kv; }
 
-// Workspace: the extend schedule (header, unit list), the partial-result
-// slots of units cut into key-range parts, then the decode split partials.
+// Workspace: the extend schedule (header, unit list, item table), the
+// partial-result slots of units cut into key-range parts, then the decode
+// split partials.
 Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int max_kv_len) {
   Layout L{};
   const int G = group_of(h_q, h_kv);
@@ -103,7 +104,8 @@ Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int m
   L.max_splits = (max_kv_len + kDecodeSplit - 1) / kDecodeSplit;
   L.header_off = 0;
   L.units_off = 256;
-  L.partial_off = L.units_off + align256(static_cast<size_t>(cap) * sizeof(UnitEntry));
+  L.items_off = L.units_off + align256(static_cast<size_t>(cap) * sizeof(UnitEntry));
+  L.partial_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(int));
   L.slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
   const size_t parts = static_cast<size_t>(n_seqs) * h_q * L.max_splits;
   L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_floats(d) * sizeof(float));
@@ -117,6 +119,7 @@ ExtendSched sched_of(const Layout& L, void* ws) {
   ExtendSched s;
   s.header = reinterpret_cast<int*>(b + L.header_off);
   s.units = reinterpret_cast<UnitEntry*>(b + L.units_off);
+  s.items = reinterpret_cast<int*>(b + L.items_off);
   s.partial = reinterpret_cast<float*>(b + L.partial_off);
   return s;
 }

@@ -13,13 +13,15 @@
 // per row: the article's online-softmax LSE merge, applied tile by tile.
 //
 // Persistent, balanced grid: one CTA per SM.  The schedule kernel lists the
-// units and cuts each into the same number of key-range parts, chosen so the
-// work items fill whole waves of CTAs; CTAs take items part-major, so the CTAs
-// working on one KV head at a time stream the same key range together (the
-// K/V tiles are read from HBM once and served to the others from L2).  With
-// more than one part, each part's normalised partial (O, m, l) goes to a
-// workspace slot and the merge kernel combines a unit's parts with the same
-// online-softmax LSE rule.
+// units and cuts each into key-range parts of about one target length, chosen
+// so the parts fill whole waves of CTAs (units of equal length get equal
+// parts); it orders the parts largest first in a few size classes, part-major
+// within a class, and deals them to the CTAs in snake order.  CTAs running at
+// the same time then stream the same key range of a KV head (the K/V tiles are
+// read from HBM once and served to the others from L2), and units of unequal
+// length still even out across CTAs.  A unit cut into several parts has each
+// part's normalised partial (O, m, l) written to a workspace slot, and the
+// merge kernel combines them with the same online-softmax LSE rule.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: both Q tiles of each unit, then the K ring
@@ -100,23 +102,26 @@ __device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxn
 struct Item {
   int seq, g, q0, E, P, kv_lo, kv_hi;
   int i0_0, i0_1, kv_end_0, kv_end_1, n_kt_0, n_kt_1;
-  bool whole;
+  bool whole;  // the unit is not cut: its output goes straight to out / lse
+  int slot;    // partial slot of this part otherwise
   __device__ __forceinline__ int i0(int t) const { return t ? i0_1 : i0_0; }
   __device__ __forceinline__ int kv_end(int t) const { return t ? kv_end_1 : kv_end_0; }
   __device__ __forceinline__ int n_kt(int t) const { return t ? n_kt_1 : n_kt_0; }
 };
 
-// Fills `it` for work item i (part i / n_units of unit i % n_units); false if
-// that part is empty (a unit with fewer key tiles than parts).
-__device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, int n_units, int parts, Item& it) {
-  const int u = i % n_units;
-  const int p = i / n_units;
+// Fills `it` for item-table entry i; false for an empty entry (or part).
+__device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, Item& it) {
+  const int item = a.sched.items[i];
+  if (item < 0) return false;
+  const int u = item & ((1 << kItemPartShift) - 1);
+  const int p = item >> kItemPartShift;
   const UnitEntry e = a.sched.units[u];
-  const int len = (e.n_kv + parts - 1) / parts;
+  const int len = (e.n_kv + e.parts - 1) / e.parts;
   it.kv_lo = p * len;
   it.kv_hi = min(it.kv_lo + len, e.n_kv);
   if (it.kv_lo >= it.kv_hi) return false;
-  it.whole = parts == 1;
+  it.whole = e.parts == 1;
+  it.slot = e.slot + p;
   it.seq = e.seq;
   it.g = e.kv_head;
   it.q0 = a.qo_indptr[e.seq];
@@ -141,11 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   Bars<NK, NV>* bars = reinterpret_cast<Bars<NK, NV>*>(smem + C::kBarOff);
 
   const int nc = a.sched.header[1];
-  const int n_units = a.sched.header[2];
-  const int parts = a.sched.header[3];
-  const int n_items = n_units * parts;
+  const int n_items = a.sched.header[3];  // item-table entries; CTA c takes c, c + nc, ...
   const int cta = blockIdx.x;
-  if (cta >= nc || cta >= n_items) return;  // CTAs without work (uniform over the CTA)
+  if (cta >= nc) return;  // CTAs without work (uniform over the CTA)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       bool ok = true;
       Item it;
       for (int wi = cta; ok && wi < n_items; wi += nc) {
-        if (!load_item(a, wi, n_units, parts, it)) continue;
+        if (!load_item(a, wi, it)) continue;
         if (is_k) {
           if (items > 0 &&
               !mbar_wait(&bars->q_empty, (items - 1) & 1, abort, a.wait_ns, a.status, kDetailQFull)) break;
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       bool ok = true;
       Item it;
       for (int wi = cta; ok && wi < n_items; wi += nc) {
-        if (!load_item(a, wi, n_units, parts, it)) continue;
+        if (!load_item(a, wi, it)) continue;
         if (!mbar_wait(&bars->q_full, items & 1, abort, a.wait_ns, a.status, kDetailQFull) ||
             !mbar_wait(&bars->k_full[kc % NK], (kc / NK) & 1, abort, a.wait_ns, a.status, kDetailKFull)) {
           ok = false;
@@ -378,16 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     bool ok = true;
     Item it;
     for (int wi = cta; ok && wi < n_items; wi += nc) {
-      if (!load_item(a, wi, n_units, parts, it)) continue;
+      if (!load_item(a, wi, it)) continue;
       const int i0t = it.i0(t);
       const int i = i0t + r / a.group;              // token index within the chunk
       const int lim = it.P + min(i, it.E - 1);    // last key this row may see
       const int jhi = min(it.kv_hi, it.n_kt(t));
       const int R = t * kBlockM + r;               // row of the unit
-      float* part = a.sched.partial + static_cast<size_t>(wi) * slot_floats;
       if (it.kv_lo >= jhi) {
         // no key tile of this portion reaches this query tile: an empty partial
         if (!it.whole) {
+          float* part = a.sched.partial + static_cast<size_t>(it.slot) * slot_floats;
           for (int c = 0; c < D; ++c) part[static_cast<size_t>(R) * D + c] = 0.f;
           part[static_cast<size_t>(kUnitRows) * D + R] = -INFINITY;
           part[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] = 0.f;
@@ -525,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           a.lse[static_cast<int64_t>(it.q0 + i) * a.h_q + head] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       } else {
         // one part of a unit: the normalised partial goes to the item's slot
+        float* part = a.sched.partial + static_cast<size_t>(it.slot) * slot_floats;
         float4* prow = reinterpret_cast<float4*>(part + static_cast<size_t>(R) * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -555,10 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 template <int D>
 __global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant__ ExtendTcArgs a) {
   const int n_units = a.sched.header[2];
-  const int parts = a.sched.header[3];
   const int u = blockIdx.x;
-  if (parts <= 1 || u >= n_units) return;
+  if (u >= n_units) return;
   const UnitEntry e = a.sched.units[u];
+  const int parts = e.parts;
+  if (parts <= 1) return;
   const int len = (e.n_kv + parts - 1) / parts;
   const int R = threadIdx.x;
   const int t = R / kBlockM;
@@ -570,7 +575,7 @@ __global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant
   const size_t slot_floats = partial_slot_floats(D);
   float M = -INFINITY;
   for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
-    const float* sl = a.sched.partial + static_cast<size_t>(p * n_units + u) * slot_floats;
+    const float* sl = a.sched.partial + static_cast<size_t>(e.slot + p) * slot_floats;
     if (sl[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] > 0.f)
       M = fmaxf(M, sl[static_cast<size_t>(kUnitRows) * D + R]);
   }
@@ -579,7 +584,7 @@ __global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant
 #pragma unroll
   for (int d = 0; d < D; ++d) o[d] = 0.f;
   for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
-    const float* sl = a.sched.partial + static_cast<size_t>(p * n_units + u) * slot_floats;
+    const float* sl = a.sched.partial + static_cast<size_t>(e.slot + p) * slot_floats;
     const float l = sl[static_cast<size_t>(kUnitRows) * D + kUnitRows + R];
     if (!(l > 0.f)) continue;  // this part holds no key of this row
     const float w = fast_exp2(sl[static_cast<size_t>(kUnitRows) * D + R] - M) * l;
@@ -648,63 +653,251 @@ __device__ int seq_tiles(const ScheduleArgs& a, int s, bool record) {
   return bad ? 0 : (E + a.tok - 1) / a.tok;
 }
 
-// Unit list (per KV head, each sequence's units last-first) and the number of
-// key-range parts per unit.
-__global__ void schedule_kernel(ScheduleArgs a) {
-  __shared__ int warp_sums[32];
-  const int n = a.seq_end - a.seq_begin;
-  int local = 0;
-  for (int k = threadIdx.x; k < n; k += blockDim.x) local += (seq_tiles(a, a.seq_begin + k, true) + 1) / 2;
-  int pairs = 0;  // units per KV head
-  block_exclusive_scan(local, &pairs, warp_sums);
-  const int n_units = min(pairs * a.h_kv, a.capacity);
-  if (pairs * a.h_kv > a.capacity && threadIdx.x == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
-  int carry = 0;
-  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
-    const int k = c0 + threadIdx.x;
-    const int s = a.seq_begin + k;
-    const int np = k < n ? (seq_tiles(a, s, false) + 1) / 2 : 0;
-    int chunk_total = 0;
-    const int off = carry + block_exclusive_scan(np, &chunk_total, warp_sums);
-    if (np > 0) {
-      const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
-      const int P = a.prefix_len[s];
-      for (int q = 0; q < np; ++q) {
-        const int pair = np - 1 - q;
-        const int i_last = min(E, (2 * pair + 2) * a.tok);  // tokens [0, i_last) of the unit's rows
-        const int n_kv = (P + i_last + kBlockN - 1) / kBlockN;
-        for (int g = 0; g < a.h_kv; ++g) {
-          const int idx = g * pairs + off + q;
-          if (idx < a.capacity) a.sched.units[idx] = UnitEntry{s, pair, g, n_kv};
-        }
-      }
+// Parts of a unit of n_kv key tiles for target part length T, and the size
+// class of a part of `size` tiles (kSizeBuckets - 1 = the largest).
+__device__ __forceinline__ int unit_parts(int n_kv, int T) { return min(kMaxParts, max(1, (n_kv + T - 1) / T)); }
+__device__ __forceinline__ int size_bucket(int size, int T) {
+  return min(kSizeBuckets - 1, size * kSizeBuckets / (T + 1));
+}
+
+constexpr int kSchedThreads = 256;
+constexpr int kSchedSeqCache = 2048;   // sequences whose pair offsets stay in shared memory
+constexpr int kSchedUnitCache = 8192;  // units whose key-tile counts stay in shared memory
+
+// Block-wide exclusive prefix sums of N per-thread counters at once (blockDim.x
+// <= 32 * 32): v is replaced by this thread's prefix, totals[] (shared) gets
+// the block totals.  Two barriers.
+template <int N>
+__device__ void block_scan_n(int (&v)[N], int (*scratch)[N], int* totals) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    int x = v[i];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
-    carry += chunk_total;
+    incl[i] = x;
+    if (lane == 31) scratch[w][i] = x;
   }
   __syncthreads();
-  // total key tiles, then the number of parts per unit: whole waves of CTAs
-  int wl = 0;
-  for (int u = threadIdx.x; u < n_units; u += blockDim.x) wl += a.sched.units[u].n_kv;
-  int W = 0;
-  block_exclusive_scan(wl, &W, warp_sums);
-  if (threadIdx.x == 0) {
-    int best = 1;
-    float best_eff = 0.f;
-    for (int p = 1; p <= kMaxParts; ++p) {
-      if (p > 1 && (p * n_units > a.max_slots || W < p * n_units * kMinTilesPerPart)) break;
-      const int items = p * n_units;
-      const int ncp = min(a.n_ctas, items);
+  if (threadIdx.x < N) {  // warp totals -> exclusive warp offsets, in place
+    int run = 0;
+    for (int k = 0; k < nw; ++k) {
+      const int t = scratch[k][threadIdx.x];
+      scratch[k][threadIdx.x] = run;
+      run += t;
+    }
+    totals[threadIdx.x] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = scratch[w][i] + incl[i] - v[i];
+  __syncthreads();  // scratch and totals may be reused after this
+}
+
+// The work list of one extend launch.
+// 1. Units: per KV head, each sequence's units last-first (the longest key
+//    range first), two query tiles each.
+// 2. Parts: candidate target lengths T = ceil(longest unit / S), S = 1..8; a
+//    unit of n_kv key tiles is cut into ceil(n_kv / T) parts.  The candidate
+//    whose parts fill whole waves of CTAs best (work / (CTAs x T x waves)) is
+//    taken; a larger S must win clearly (3 %), fit the partial slots and keep
+//    parts of kMinTilesPerPart tiles on average.  Units of equal length thus
+//    get the same number of parts; unequal ones get parts of similar length.
+// 3. Order: parts in kSizeBuckets size classes, largest first; within a class
+//    part-major, then unit order (so CTAs running at the same time stream the
+//    same key range of a KV head).  Position k of that order goes to CTA
+//    k mod nc in even waves and nc - 1 - k mod nc in odd ones (snake order),
+//    which evens out the CTAs' totals.
+__global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs a) {
+  constexpr int kRuns = kMaxParts * kSizeBuckets;  // (part, size class) counters
+  __shared__ int warp_sums[32];
+  __shared__ int scratch[32][kRuns];
+  __shared__ int totals[kRuns];
+  __shared__ int run_start[kRuns];
+  __shared__ int s_seq_off[kSchedSeqCache + 1];
+  __shared__ int s_nkv[kSchedUnitCache];
+  __shared__ int s_T, s_items;
+  const int tid = threadIdx.x;
+  const int n = a.seq_end - a.seq_begin;
+  // pair offsets per sequence (exclusive) and their total; the item table is
+  // scratch for them when there are too many sequences for shared memory
+  const bool seq_cached = n <= kSchedSeqCache;
+  int* seq_off = seq_cached ? s_seq_off : a.sched.items;
+  int carry = 0;
+  for (int c0 = 0; c0 < n; c0 += blockDim.x) {
+    const int k = c0 + tid;
+    const int np = k < n ? (seq_tiles(a, a.seq_begin + k, true) + 1) / 2 : 0;
+    int chunk_total = 0;
+    const int off = carry + block_exclusive_scan(np, &chunk_total, warp_sums);
+    if (k < n) seq_off[k] = off;
+    carry += chunk_total;
+  }
+  const int pairs = carry;  // units per KV head
+  if (tid == 0) seq_off[n] = pairs;
+  const int n_units = min(pairs * a.h_kv, a.capacity);
+  if (pairs * a.h_kv > a.capacity && tid == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
+  const bool unit_cached = n_units <= kSchedUnitCache;
+  __syncthreads();
+  // 1. units (each thread a contiguous range, so unit order is thread order)
+  const int per = (n_units + blockDim.x - 1) / blockDim.x;
+  const int u_lo = min(n_units, tid * per), u_hi = min(n_units, u_lo + per);
+  auto n_kv_of = [&](int u) { return unit_cached ? s_nkv[u] : a.sched.units[u].n_kv; };
+  int W_local = 0, max_local = 0;
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int g = u / pairs;
+    const int r = u - g * pairs;
+    int lo = 0, hi = n;  // the sequence k with seq_off[k] <= r < seq_off[k + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) / 2;
+      if (seq_off[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int s = a.seq_begin + lo;
+    const int np = seq_off[lo + 1] - seq_off[lo];
+    const int pair = np - 1 - (r - seq_off[lo]);
+    const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
+    const int P = a.prefix_len[s];
+    const int i_last = min(E, (2 * pair + 2) * a.tok);  // tokens [0, i_last) of the unit's rows
+    const int n_kv = (P + i_last + kBlockN - 1) / kBlockN;
+    a.sched.units[u] = UnitEntry{s, pair, g, n_kv, 1, 0};
+    if (unit_cached) s_nkv[u] = n_kv;
+    W_local += n_kv;
+    max_local = max(max_local, n_kv);
+  }
+  // total key tiles and the longest unit
+  {
+    const int wsum = __reduce_add_sync(0xffffffffu, W_local);
+    const int wmax = __reduce_max_sync(0xffffffffu, max_local);
+    if ((tid & 31) == 0) {
+      scratch[tid >> 5][0] = wsum;
+      scratch[tid >> 5][1] = wmax;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int t = 0, m = 0;
+      for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) {
+        t += scratch[k][0];
+        m = max(m, scratch[k][1]);
+      }
+      totals[0] = t;
+      totals[1] = m;
+    }
+    __syncthreads();
+  }
+  const int W = totals[0];
+  const int n_max = totals[1];
+  __syncthreads();
+  // 2. parts: items and partial slots each candidate S would need
+  int v16[2 * kMaxParts] = {};
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int n_kv = n_kv_of(u);
+#pragma unroll
+    for (int S = 1; S <= kMaxParts; ++S) {
+      const int pc = unit_parts(n_kv, max(1, (n_max + S - 1) / S));
+      v16[S - 1] += pc;
+      v16[kMaxParts + S - 1] += pc > 1 ? pc : 0;
+    }
+  }
+  block_scan_n<2 * kMaxParts>(v16, reinterpret_cast<int (*)[2 * kMaxParts]>(&scratch[0][0]), totals);
+  const int* sums16 = totals;
+  if (tid == 0) {
+    int best_T = max(1, n_max);
+    float best_eff = -1.f;
+    for (int S = 1; S <= kMaxParts; ++S) {
+      const int T = max(1, (n_max + S - 1) / S);
+      const int items = sums16[S - 1];
+      if (S > 1 && (sums16[kMaxParts + S - 1] > a.max_slots || W < items * kMinTilesPerPart)) break;
+      const int ncp = max(1, min(a.n_ctas, items));
       const int waves = (items + ncp - 1) / ncp;
-      const float eff = static_cast<float>(items) / static_cast<float>(waves * ncp);
+      const float eff = static_cast<float>(W) / (static_cast<float>(ncp) * T * waves);
       if (eff > best_eff + 0.03f) {  // more parts only when they fill the waves clearly better
-        best = p;
+        best_T = T;
         best_eff = eff;
       }
     }
+    s_T = best_T;
+  }
+  __syncthreads();
+  const int T = s_T;
+  // 3. parts and partial slots per unit (slots in unit order, split units only)
+  int slots_local = 0;
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int pc = unit_parts(n_kv_of(u), T);
+    slots_local += pc > 1 ? pc : 0;
+  }
+  int slot_total = 0;
+  int slot = block_exclusive_scan(slots_local, &slot_total, warp_sums);
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int pc = unit_parts(n_kv_of(u), T);
+    a.sched.units[u].parts = pc;
+    a.sched.units[u].slot = pc > 1 ? slot : 0;
+    slot += pc > 1 ? pc : 0;
+  }
+  // item counts per (part, size class); this thread's prefix in each run
+  int cnt[kRuns] = {};
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int n_kv = n_kv_of(u);
+    const int pc = unit_parts(n_kv, T);
+    const int len = (n_kv + pc - 1) / pc;
+#pragma unroll
+    for (int p = 0; p < kMaxParts; ++p) {
+      const int size = min(len, n_kv - p * len);
+      const int b = size_bucket(max(size, 0), T);
+#pragma unroll
+      for (int q = 0; q < kSizeBuckets; ++q) cnt[p * kSizeBuckets + q] += (p < pc && size > 0 && b == q) ? 1 : 0;
+    }
+  }
+  block_scan_n<kRuns>(cnt, scratch, totals);
+  // start of each (part, class) run in the largest-first order
+  if (tid == 0) {
+    int pos = 0;
+    for (int b = kSizeBuckets - 1; b >= 0; --b)
+      for (int p = 0; p < kMaxParts; ++p) {
+        run_start[p * kSizeBuckets + b] = pos;
+        pos += totals[p * kSizeBuckets + b];
+      }
+    s_items = pos;
+  }
+  __syncthreads();
+  const int n_items = s_items;
+  const int nc = n_items > 0 ? min(a.n_ctas, n_items) : 0;
+  const int table_len = nc > 0 ? (n_items + nc - 1) / nc * nc : 0;
+  // the last wave's unused entries read as empty: its low CTAs' entries when
+  // that wave runs backwards (odd), its high ones otherwise
+  if (table_len > n_items) {
+    const int last = table_len / nc - 1;
+    const int rem = n_items - last * nc;
+    const int e0 = last * nc + ((last & 1) ? 0 : rem);
+    for (int i = e0 + tid; i < e0 + (nc - rem); i += blockDim.x) a.sched.items[i] = -1;
+  }
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int n_kv = n_kv_of(u);
+    const int pc = unit_parts(n_kv, T);
+    const int len = (n_kv + pc - 1) / pc;
+#pragma unroll
+    for (int p = 0; p < kMaxParts; ++p) {
+      const int size = min(len, n_kv - p * len);
+      if (p >= pc || size <= 0) continue;
+      const int b = size_bucket(size, T);
+      int k = 0;  // this item's position: its run's start plus the items before it in the run
+#pragma unroll
+      for (int q = 0; q < kSizeBuckets; ++q)
+        if (b == q) k = run_start[p * kSizeBuckets + q] + cnt[p * kSizeBuckets + q]++;
+      const int wave = k / nc, pos = k - wave * nc;
+      const int cta = (wave & 1) ? nc - 1 - pos : pos;
+      a.sched.items[wave * nc + cta] = u | (p << kItemPartShift);
+    }
+  }
+  if (tid == 0) {
     a.sched.header[0] = W;
-    a.sched.header[1] = n_units > 0 ? min(a.n_ctas, best * n_units) : 0;
+    a.sched.header[1] = nc;
     a.sched.header[2] = n_units;
-    a.sched.header[3] = best;
+    a.sched.header[3] = table_len;
+    a.sched.header[4] = T;
+    a.sched.header[5] = n_items;
   }
 }
 
@@ -715,7 +908,7 @@ size_t extend_tc_smem_bytes(int d) {
 }
 
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
-  schedule_kernel<<<1, 1024, 0, s>>>(a);
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,8 @@ constexpr int kDecodeSplit = 2048;  // keys per decode split
 constexpr int kMaxCtas = 160;        // upper bound of the persistent extend grid (SMs used)
 constexpr int kMaxParts = 8;         // key-range parts a unit may be cut into
 constexpr int kMinTilesPerPart = 4;  // parts shorter than this (on average) are not used
+constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first order
+constexpr int kItemPartShift = 24;   // item = unit | part << kItemPartShift
 constexpr int kMaxSlots = 1024;      // partial-result slots in the workspace
 constexpr int kUnitRows = 2 * kBlockM;
 
@@ -24,15 +26,21 @@ struct UnitEntry {  // one extend work unit: two query tiles of one sequence and
   int pair;      // query tiles 2*pair and 2*pair+1 of the sequence
   int kv_head;
   int n_kv;      // key tiles the unit needs
+  int parts;     // key-range parts the unit is cut into (1: it writes its output directly)
+  int slot;      // partial slot of its part 0 (parts > 1); part p uses slot + p
 };
 
-// Device-side schedule kept in the caller's workspace.  Work item i is part
-// p = i / n_units of unit u = i % n_units: key tiles [p*len, min((p+1)*len, n_kv))
-// with len = ceil(n_kv / parts).  CTA c takes items c, c + n_ctas, ...
+// Device-side schedule kept in the caller's workspace.  Unit u is cut into
+// units[u].parts parts; part p covers key tiles [p*len, min((p+1)*len, n_kv))
+// with len = ceil(n_kv / parts).  The item table lists the non-empty parts
+// (unit | part << kItemPartShift, -1 for none); CTA c takes table entries
+// c, c + header[1], ...
 struct ExtendSched {
-  int* header;          // [0] total key tiles, [1] CTAs used, [2] units, [3] parts per unit
+  int* header;          // [0] total key tiles, [1] CTAs used, [2] units, [3] item table length
+                        // (a multiple of [1]), [4] target part length, [5] items
   UnitEntry* units;     // [capacity]
-  float* partial;       // [parts * units] slots: O [256 x d] (normalised), m [256] (log2), l [256]
+  int* items;           // [item capacity]
+  float* partial;       // slots: O [256 x d] (normalised), m [256] (log2), l [256]
 };
 
 __host__ __device__ constexpr size_t partial_slot_floats(int d) { return size_t(kUnitRows) * d + 2 * kUnitRows; }

@@ -62,12 +62,36 @@ class MixedSpec:
     page_size: int = PAGE_SIZE
 
 
+@dataclass(frozen=True)
+class ScheduledSpec:
+    """One scheduling step over running and waiting requests under one budget:
+    ``n_decode`` decode requests (context L ~ U[ctx_lo, ctx_hi], seeded), then
+    the running prefill continuations ``running_prefill`` = ((computed, need),
+    ...), then the waiting queue ``waiting`` = ((cached, prompt), ...)."""
+    name: str
+    seed: int
+    token_budget: int
+    n_decode: int
+    ctx_lo: int
+    ctx_hi: int
+    running_prefill: tuple
+    waiting: tuple
+    h_q: int
+    h_kv: int
+    d: int
+    dtype: torch.dtype
+    std: float = 0.5
+    page_size: int = PAGE_SIZE
+
+
 CONFIGS = {
     "cfg1": ChunkedSpec("cfg1", 1, 512, 0.0, 128, 4, 4, 64, torch.float32, std=1.0, prefix_std=1.0),
     "cfg2": ChunkedSpec("cfg2", 2, 4000, 0.0, 512, 32, 8, 128, torch.bfloat16),
     "cfg3": ChunkedSpec("cfg3", 3, 32768, 0.5, 8192, 32, 8, 128, torch.bfloat16, prefix_std=1.0),
     "cfg4": MixedSpec("cfg4", 4, 2304, 256, 512, 32768, 30720, 4096, 32, 8, 128, torch.bfloat16),
     "cfg5": ChunkedSpec("cfg5", 5, 131072, 0.0, 1024, 64, 8, 128, torch.bfloat16),
+    "sched": ScheduledSpec("sched", 6, 8192, 64, 512, 32768, ((8192, 2048), (30720, 2048), (65536, 2048)),
+                           ((4096, 16384), (0, 4000)), 32, 8, 128, torch.bfloat16),
 }
 
 WORKLOAD_TEXT = {
@@ -77,6 +101,9 @@ WORKLOAD_TEXT = {
     "cfg4": "mixed step budget 2304: prefill E=2048 at P=30720 + 256 decode rows L~U[512,32768], "
             "GQA 32/8, d=128, bf16, permuted pages",
     "cfg5": "one request N=131072, chunk 1024 (128 chunks), GQA 64/8, d=128, bf16, page 16",
+    "sched": "one scheduling step, budget 8192: 64 decode rows L~U[512,32768], running prefills at "
+             "P=8192/30720/65536 (2048 tokens each), waiting prompts 16384 (4096 cached, cut to 1984) and 4000 "
+             "(left queued); GQA 32/8, d=128, bf16, permuted pages",
 }
 
 
@@ -228,3 +255,50 @@ def sample_rows(n_rows: int, tile_rows: int, count: int, seed: int) -> list:
             break
         picks.add(r)
     return sorted(x for x in picks if 0 <= x < n_rows)
+
+
+def scheduled_requests(spec: ScheduledSpec) -> tuple[list, list]:
+    """The step's queues: running = decode requests (L-1 cached, 1 needed) then
+    the running prefill continuations; waiting = (cached, prompt) per request."""
+    g = torch.Generator().manual_seed(spec.seed)
+    ctx = torch.randint(spec.ctx_lo, spec.ctx_hi + 1, (spec.n_decode,), generator=g).tolist()
+    running = [(L - 1, 1) for L in ctx] + [tuple(x) for x in spec.running_prefill]
+    return running, [tuple(x) for x in spec.waiting]
+
+
+@dataclass
+class ScheduledBatch:
+    """Inputs of one scheduled step for a given batch layout ``lens`` =
+    [(prefix_len, query_len)] per sequence in batch order: a shared page pool
+    (seeded permutation, every page filled with N(0,1)*std, so each sequence's
+    first prefix_len slots read as its cached K/V), and q/k_new/v_new rows in
+    batch row order."""
+    lens: list
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    page_table: torch.Tensor
+    page_table_host: torch.Tensor
+
+
+def make_scheduled(spec: ScheduledSpec, lens: list, device="cpu") -> ScheduledBatch:
+    gen = torch.Generator(device=device)
+    gen.manual_seed(spec.seed + 1000)
+    npages = [_pages(P + E, spec.page_size) for P, E in lens]
+    total_pages = sum(npages)
+    perm = torch.randperm(total_pages, generator=gen, device=device).to(torch.int32).cpu()
+    pt = torch.full((len(lens), max(npages)), -1, dtype=torch.int32)
+    off = 0
+    for s, n in enumerate(npages):
+        pt[s, :n] = perm[off:off + n]
+        off += n
+    shape_c = (total_pages, spec.page_size, spec.h_kv, spec.d)
+    k_cache = _randn(gen, shape_c, spec.std, spec.dtype, device)
+    v_cache = _randn(gen, shape_c, spec.std, spec.dtype, device)
+    rows = sum(E for _, E in lens)
+    q = _randn(gen, (rows, spec.h_q, spec.d), spec.std, spec.dtype, device)
+    k_new = _randn(gen, (rows, spec.h_kv, spec.d), spec.std, spec.dtype, device)
+    v_new = _randn(gen, (rows, spec.h_kv, spec.d), spec.std, spec.dtype, device)
+    return ScheduledBatch(list(lens), q, k_new, v_new, k_cache, v_cache, pt.to(device), pt)
