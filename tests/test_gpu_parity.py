@@ -303,6 +303,36 @@ def test_scheduled_step_pages_example_sampled(cpe):
         np.testing.assert_allclose(lse[qo[s]:qo[s + 1]][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 
+def test_sched_workload_sampled(cpe):
+    """The scheduled-step bench workload at full size, as the bench runs it:
+    decode rows (shortest, longest, a seeded sample) and sampled rows of each
+    prefill chunk, whose units the scheduler cuts into unequal part counts."""
+    spec = W.CONFIGS["sched"]
+    running, waiting = W.scheduled_requests(spec)
+    plan = cpe.cpe_plan_schedule(spec.token_budget, running, waiting)
+    assert plan == oracle.plan_schedule(spec.token_budget, running, waiting)
+    qo = plan["qo_indptr"]
+    lens = [(p, qo[i + 1] - qo[i]) for i, p in enumerate(plan["prefix_len"])]
+    mb = W.make_scheduled(spec, lens, device="cuda")
+    nd = plan["n_decode"]
+    lse = torch.empty(mb.q.shape[0], spec.h_q, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(mb.q, mb.k_new, mb.v_new, mb.k_cache, mb.v_cache, mb.page_table, i32(qo),
+                                i32(plan["prefix_len"]), nd, max(plan["kv_len"]), lse=lse)
+    _status_ok(cpe)
+    g = torch.Generator().manual_seed(606)
+    order = sorted(range(nd), key=lambda s: plan["kv_len"][s])
+    seqs = sorted(set([order[0], order[-1]] + torch.randperm(nd, generator=g)[:4].tolist())) + list(range(nd, len(lens)))
+    for s in seqs:
+        E = qo[s + 1] - qo[s]
+        rows = [0] if E == 1 else W.sample_rows(E, 32, 40, 700 + s)
+        kc, vc, pt = extract_pages(mb.k_cache, mb.v_cache, mb.page_table_host, [s], [plan["kv_len"][s]])
+        q = mb.q[qo[s]:qo[s + 1]].cpu()
+        ref_o, ref_l = oracle.extend_attention(q, kc, vc, pt, [0, E], [plan["prefix_len"][s]], spec.h_q, spec.h_kv,
+                                               rows=rows)
+        check_close(out[qo[s]:qo[s + 1]][rows], ref_o, f"sched sequence {s}")
+        np.testing.assert_allclose(lse[qo[s]:qo[s + 1]][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
 # ---------------------------------------------------------------- device-side errors
 
 def test_bad_page_id_is_reported(cpe):
