@@ -12,6 +12,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+from typing import NamedTuple
 from dataclasses import dataclass
 
 import torch
@@ -28,7 +29,8 @@ CPE_F32, CPE_BF16 = 0, 1
 EXPORTS = ["cpe_plan_chunks", "cpe_plan_budget", "cpe_plan_mixed_step", "cpe_plan_schedule", "cpe_kv_append",
            "cpe_workspace_size", "cpe_extend_attention", "cpe_mixed_step", "cpe_decode_attention",
            "cpe_get_device_status", "cpe_set_wait_limit_ns", "cpe_status_string", "cpe_last_error",
-           "cpe_launch_count", "cpe_decode_attention_noalloc"]
+           "cpe_launch_count", "cpe_decode_attention_noalloc", "cpe_decide_decode_first",
+           "cpe_simulate_requests"]
 
 _vp, _i32, _i64, _f32, _f64, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                     ctypes.c_double, ctypes.c_size_t)
@@ -46,6 +48,19 @@ _lib.cpe_plan_mixed_step.argtypes = [_i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp,
                                      ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
 _lib.cpe_plan_schedule.argtypes = [_i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, ctypes.POINTER(_i32), _vp, _vp, _vp,
                                    _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
+_LATENCY_FN = ctypes.CFUNCTYPE(ctypes.c_double, _vp, _i32, _i32, _i32, _i32)
+_DECIDE_FN = ctypes.CFUNCTYPE(_i32, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32))
+_MERGE_FN = ctypes.CFUNCTYPE(ctypes.c_double, _vp, ctypes.c_double, ctypes.c_double)
+
+
+class _SimResult(ctypes.Structure):
+    _fields_ = [("ttft_ms", _f64), ("tpot_ms", _f64), ("makespan_ms", _f64), ("request_throughput", _f64),
+                ("output_throughput", _f64), ("steps", _i64)]
+
+
+_lib.cpe_decide_decode_first.argtypes = [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
+_lib.cpe_simulate_requests.argtypes = [_i32, _vp, _vp, _i32, _i32, _i32, _LATENCY_FN, _vp, _DECIDE_FN, _MERGE_FN, _vp,
+                                       _vp, _vp, ctypes.POINTER(_SimResult)]
 _lib.cpe_kv_append.argtypes = [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                _i32, ctypes.c_int, _vp]
 _lib.cpe_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
@@ -161,6 +176,58 @@ def cpe_plan_schedule(token_budget: int, running, waiting):
     k = ns.value
     return {"granted": list(granted[:n]), "n_admitted": adm.value, "qo_indptr": list(qo[:k + 1]),
             "prefix_len": list(pl[:k]), "kv_len": list(kv[:k]), "seq_request": list(sr[:k]), "n_decode": nd.value}
+
+
+class SchedulerState(NamedTuple):
+    """What a scheduler sees at each simulated step."""
+    ready_decode: int
+    pending_prefill: int
+    chunk_query_len: int
+    max_batched_tokens: int
+
+
+class StepDecision(NamedTuple):
+    p_step: int
+    d_step: int
+
+
+def cpe_decide_decode_first(max_batched_tokens: int, ready_decode: int, pending_prefill: int, chunk_query_len: int,
+                            slack_percent: int = 115) -> StepDecision:
+    p, d = _i32(0), _i32(0)
+    _check(_lib.cpe_decide_decode_first(max_batched_tokens, ready_decode, pending_prefill, chunk_query_len,
+                                        slack_percent, ctypes.byref(p), ctypes.byref(d)), "cpe_decide_decode_first")
+    return StepDecision(p.value, d.value)
+
+
+def cpe_simulate_requests(chunks, n_requests: int, output_len: int, max_batched_tokens: int, latency,
+                          scheduler=None) -> dict:
+    """Time simulation of n_requests requests with chunk plan ``chunks`` =
+    [(query_len, seq_len)].  latency(is_decode, batch, query_len, seq_len) -> ms.
+    scheduler: None (decode-first with 15 % slack) or an object with
+    decide(SchedulerState) -> StepDecision and step_latency(prefill_ms, decode_ms)."""
+    n = len(chunks)
+    ql = (_i32 * max(1, n))(*[q for q, _ in chunks])
+    sl = (_i32 * max(1, n))(*[x for _, x in chunks])
+    lat = _LATENCY_FN(lambda ctx, d, b, q, x: float(latency(bool(d), b, q, x)))
+    dec, mrg = _DECIDE_FN(), _MERGE_FN()
+    if scheduler is not None:
+        def _decide(ctx, ready, pending, qlen, B, p, d):
+            try:
+                r = scheduler.decide(SchedulerState(ready, pending, qlen, B))
+                p[0], d[0] = int(r.p_step), int(r.d_step)
+                return 0
+            except Exception:  # reported to the caller as a failed scheduler
+                return 1
+        dec = _DECIDE_FN(_decide)
+        mrg = _MERGE_FN(lambda ctx, a, b: float(scheduler.step_latency(a, b)))
+    first = (_f64 * max(1, n_requests))()
+    fin = (_f64 * max(1, n_requests))()
+    res = _SimResult()
+    _check(_lib.cpe_simulate_requests(n, ql, sl, n_requests, output_len, max_batched_tokens, lat, None, dec, mrg,
+                                      None, first, fin, ctypes.byref(res)), "cpe_simulate_requests")
+    return {"ttft": res.ttft_ms, "tpot": res.tpot_ms, "makespan": res.makespan_ms,
+            "request_throughput": res.request_throughput, "output_throughput": res.output_throughput,
+            "steps": res.steps, "first_token_time": list(first[:n_requests]), "finish_time": list(fin[:n_requests])}
 
 
 def cpe_workspace_size(n_seqs: int, total_q: int, h_q: int, h_kv: int, d: int, max_kv_len: int) -> int:

@@ -170,6 +170,74 @@ cpe_status cpe_plan_schedule(int32_t token_budget, int32_t n_running, const int3
                              int32_t* n_seqs, int32_t* n_decode);
 
 /*
+ * cpe_decide_decode_first — one step decision of the decode-first scheduler
+ * with slack (host only).
+ *   msmodeling chunked-prefill RFC, section 3.1.4 (DecodeFirstWithSlack):
+ *   limit = floor(B * slack_percent / 100) (integer arithmetic; 115 for the
+ *   RFC's 15 % slack), d_step = min(ready_decode, B),
+ *   p_step = max(0, min(pending_prefill, floor((limit - d_step) / chunk_query_len))).
+ * Errors: CPE_ERR_INVALID_ARG for B <= 0, chunk_query_len <= 0,
+ * slack_percent < 100, negative counts or null outputs.
+ */
+cpe_status cpe_decide_decode_first(int32_t max_batched_tokens, int32_t ready_decode, int32_t pending_prefill,
+                                   int32_t chunk_query_len, int32_t slack_percent, int32_t* p_step,
+                                   int32_t* d_step);
+
+/* Latency model of the time simulation: milliseconds of one prefill step of
+ * `batch` requests running a chunk of query_len tokens at context seq_len
+ * (is_decode 0), or of one decode step of `batch` requests whose mean context
+ * is seq_len (is_decode 1, query_len 1). */
+typedef double (*cpe_latency_fn)(void* ctx, int32_t is_decode, int32_t batch, int32_t query_len,
+                                 int32_t seq_len);
+/* Scheduler of the time simulation: writes the step's prefill and decode
+ * request counts for the state; returns 0 on success. */
+typedef int32_t (*cpe_decide_fn)(void* ctx, int32_t ready_decode, int32_t pending_prefill,
+                                 int32_t chunk_query_len, int32_t max_batched_tokens, int32_t* p_step,
+                                 int32_t* d_step);
+/* How the scheduler combines a step's prefill and decode latencies. */
+typedef double (*cpe_merge_fn)(void* ctx, double prefill_ms, double decode_ms);
+
+typedef struct cpe_sim_result {
+  double ttft_ms;             /* mean first-token time */
+  double tpot_ms;             /* mean time per output token after the first (0 if output_len == 1) */
+  double makespan_ms;         /* last request's finish time */
+  double request_throughput;  /* requests per second over the makespan */
+  double output_throughput;   /* output tokens per second over the makespan */
+  int64_t steps;
+} cpe_sim_result;
+
+/*
+ * cpe_simulate_requests — lightweight time simulation of n_requests identical
+ * requests entering together (host only).
+ *   msmodeling chunked-prefill RFC, section 3.1.5.  Each step asks the
+ *   scheduler for (p_step, d_step) given the ready decode requests and the
+ *   pending group: the requests at the chunk of the earliest request still in
+ *   prefill (earlier requests run their chunks first).  The earliest requests
+ *   of the group prefill and the earliest ready requests (by first-token
+ *   time) decode one token; the step lasts merge(prefill latency, decode
+ *   latency).  A request's last chunk produces its first token; it then needs
+ *   max(output_len - 1, 0) decode steps, the first at context seq_len of the
+ *   last chunk + 1.  The decode latency gets the decode batch's mean context,
+ *   rounded up.  No barrier separates prefill from decode.
+ * chunk_query_len[n_chunks], chunk_seq_len[n_chunks] (host): one request's
+ *   chunk plan.  latency (required) with latency_ctx.  decide and merge
+ *   (nullable, with sched_ctx): NULL decide means the decode-first scheduler
+ *   with 15 % slack, NULL merge the larger of the two latencies.
+ * first_token_ms[n_requests], finish_ms[n_requests] (host, nullable) receive
+ * each request's times; *out the metrics.
+ * Counts the scheduler returns beyond the pending group or the ready requests
+ * are clamped to them.
+ * Errors: CPE_ERR_INVALID_ARG for empty or non-positive lengths, a null
+ * latency or out, a scheduler that fails or schedules nothing, or a negative
+ * latency; CPE_ERR_CAPACITY if the simulation exceeds 2^31 steps.
+ */
+cpe_status cpe_simulate_requests(int32_t n_chunks, const int32_t* chunk_query_len, const int32_t* chunk_seq_len,
+                                 int32_t n_requests, int32_t output_len, int32_t max_batched_tokens,
+                                 cpe_latency_fn latency, void* latency_ctx, cpe_decide_fn decide,
+                                 cpe_merge_fn merge, void* sched_ctx, double* first_token_ms, double* finish_ms,
+                                 cpe_sim_result* out);
+
+/*
  * cpe_kv_append — write the round's new K/V rows into the paged caches.
  *   SGLang article, implementation section (the request's req_to_token row
  *   keeps its page slots across chunks); mini-infer article, write_prefill_kv.

@@ -137,3 +137,73 @@ def test_workspace_size_is_monotone_and_zero_for_bad_sizes():
     b = cpe.cpe_workspace_size(257, 2304, 32, 8, 128, 32768)
     assert 0 < a < b and b % 256 == 0
     assert cpe.cpe_workspace_size(0, 1, 32, 8, 128, 10) == 0
+
+
+def test_decide_decode_first_matches_oracle_and_pages():
+    from oracle import sched_sim
+    golden = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "sched_vectors.json")))
+    for c in golden["decide"]:
+        assert cpe.cpe_decide_decode_first(c["max_batched_tokens"], c["ready_decode"], c["pending_prefill"],
+                                           c["chunk_query_len"]) == (c["p_step"], c["d_step"])
+    rng = random.Random(13)
+    sch = sched_sim.DecodeFirstWithSlack()
+    for _ in range(500):
+        B = rng.randint(1, 9000)
+        st = sched_sim.SchedulerState(rng.randint(0, 12000), rng.randint(0, 50), rng.randint(1, B), B)
+        want = sch.decide(st)
+        assert tuple(cpe.cpe_decide_decode_first(B, st.ready_decode, st.pending_prefill, st.chunk_query_len)) == \
+            (want.p_step, want.d_step)
+    with pytest.raises(cpe.CpeError):
+        cpe.cpe_decide_decode_first(0, 1, 1, 1)
+
+
+def test_simulate_requests_matches_oracle():
+    """The native simulation gives bit-identical times to the oracle's for the
+    same latency model, with the default and with an injected scheduler."""
+    from oracle import sched_sim
+
+    class PrefillFirst:
+        def decide(self, st):
+            if st.pending_prefill:
+                return sched_sim.StepDecision(st.pending_prefill, 0)
+            return sched_sim.StepDecision(0, min(st.ready_decode, st.max_batched_tokens))
+
+        def step_latency(self, p, d):
+            return p + d
+
+    rng = random.Random(14)
+    for trial in range(40):
+        B = rng.choice([128, 512, 2048, 4000])
+        n_in = rng.randint(1, 12000)
+        chunks, done = [], 0
+        while done < n_in:
+            q = min(B, n_in - done)
+            done += q
+            chunks.append((q, done))
+        N, O = rng.randint(1, 60), rng.randint(1, 40)
+        lat = lambda d, b, q, s: (0.25 + 3e-5 * b * s) if d else (0.5 + 2e-8 * b * q * s)
+        sch = PrefillFirst() if trial % 4 == 3 else None
+        a = cpe.cpe_simulate_requests(chunks, N, O, B, lat, sch)
+        b = sched_sim.simulate(chunks, N, O, B, lat, sch)
+        for k in ("makespan", "steps", "first_token_time", "finish_time"):
+            assert a[k] == b[k], (trial, k)
+        # means: Python's float sum() compensates rounding, the native loop adds plainly
+        for k in ("ttft", "tpot", "request_throughput", "output_throughput"):
+            assert a[k] == pytest.approx(b[k], rel=1e-12, abs=1e-12), (trial, k)
+
+
+def test_simulate_requests_errors():
+    lat = lambda d, b, q, s: 1.0
+    with pytest.raises(cpe.CpeError):
+        cpe.cpe_simulate_requests([], 1, 1, 10, lat)
+    with pytest.raises(cpe.CpeError):
+        cpe.cpe_simulate_requests([(5, 5)], 1, 1, 10, lambda d, b, q, s: -1.0)
+
+    class Idle:
+        def decide(self, st):
+            return (0, 0)
+
+        def step_latency(self, p, d):
+            return 0.0
+    with pytest.raises(cpe.CpeError):
+        cpe.cpe_simulate_requests([(5, 5)], 2, 2, 10, lat, Idle())
