@@ -183,9 +183,24 @@ cpe_status validate(const char* fn, const Common& c, bool need_qo) {
   return CPE_OK;
 }
 
+// Split-KV decode of sequences [0, n_dec), one query row each.
+DecodeArgs decode_args(const Common& c, const Layout& L, int n_dec, bool use_qo, int* status) {
+  DecodeArgs a{};
+  a.q = c.q; a.k_cache = c.k_cache; a.v_cache = c.v_cache; a.page_table = c.page_table;
+  a.qo_indptr = use_qo ? c.qo_indptr : nullptr; a.prefix_len = c.prefix_len; a.out = c.out; a.lse = c.lse;
+  a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(c.workspace) + L.part_o_off);
+  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(c.workspace) + L.part_ml_off);
+  a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages; a.n_seqs = n_dec; a.seq_begin = 0;
+  a.h_q = c.h_q; a.h_kv = c.h_kv; a.d = c.d; a.max_kv_len = c.max_kv_len; a.max_splits = L.max_splits;
+  a.scale_log2 = c.sm_scale * 1.4426950408889634f;
+  return a;
+}
+
 // Extend path over sequences [seq_begin, n_seqs), whose rows are [row_begin, total_q).
+// With dec_rows > 0 (a mixed step, bf16) the decode rows [0, dec_rows) run in the
+// same persistent launch on the CTAs the extend part leaves free.
 cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_begin, int* status,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, int dec_rows = 0) {
   if (c.total_q - row_begin <= 0 || seq_begin >= c.n_seqs) return CPE_OK;
   const Layout L = workspace_layout(c.n_seqs, c.total_q, c.h_q, c.h_kv, c.d, c.max_kv_len);
   cudaError_t e;
@@ -217,6 +232,9 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   sa.qo_indptr = c.qo_indptr; sa.prefix_len = c.prefix_len; sa.seq_begin = seq_begin; sa.seq_end = c.n_seqs;
   sa.tok = tok; sa.h_kv = c.h_kv; sa.max_kv_len = c.max_kv_len; sa.max_pages = c.max_pages;
   sa.capacity = cap; sa.n_ctas = n_ctas; sa.max_slots = L.slots; sa.sched = sched; sa.status = status;
+  sa.d = c.d;
+  sa.dec_rows = dec_rows;
+  sa.dec_bytes_per_key = static_cast<int64_t>(c.h_kv) * c.d * 2 * 2;
   e = launch_schedule(sa, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 1;
@@ -236,25 +254,26 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   a.wait_ns = static_cast<uint64_t>(g_wait_ns.load() < 0 ? 0 : g_wait_ns.load());
   a.n_ctas = n_ctas;
   a.max_units = cap;
+  if (dec_rows > 0) {
+    a.dec = decode_args(c, L, dec_rows, true, status);
+    a.dec_items = dec_rows * c.h_kv * L.max_splits;
+  }
   e = launch_extend_tc(a, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 2;  // the extend kernel and the merge of key-range parts
+  if (dec_rows > 0 && L.max_splits > 1) {
+    e = launch_decode_merge(a.dec, stream);
+    if (e != cudaSuccess) return cuda_fail(fn, e);
+    g_launches += 1;
+  }
   return CPE_OK;
 }
 
 cpe_status run_decode(const char* fn, const Common& c, int n_dec, bool use_qo, int* status, cudaStream_t stream) {
   if (n_dec <= 0) return CPE_OK;
   const Layout L = workspace_layout(c.n_seqs, c.total_q, c.h_q, c.h_kv, c.d, c.max_kv_len);
-  cudaError_t e;
-  DecodeArgs a{};
-  a.q = c.q; a.k_cache = c.k_cache; a.v_cache = c.v_cache; a.page_table = c.page_table;
-  a.qo_indptr = use_qo ? c.qo_indptr : nullptr; a.prefix_len = c.prefix_len; a.out = c.out; a.lse = c.lse;
-  a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(c.workspace) + L.part_o_off);
-  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(c.workspace) + L.part_ml_off);
-  a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages; a.n_seqs = n_dec; a.seq_begin = 0;
-  a.h_q = c.h_q; a.h_kv = c.h_kv; a.d = c.d; a.max_kv_len = c.max_kv_len; a.max_splits = L.max_splits;
-  a.scale_log2 = c.sm_scale * 1.4426950408889634f;
-  e = launch_decode(a, stream);
+  const DecodeArgs a = decode_args(c, L, n_dec, use_qo, status);
+  const cudaError_t e = launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += L.max_splits > 1 ? 2 : 1;
   return CPE_OK;
@@ -387,7 +406,13 @@ cpe_status cpe_mixed_step(const void* q, const void* k_new, const void* v_new, v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // fp32 data: the CUDA-core path computes every row, decode rows included
   if (dtype == CPE_F32) return run_extend(fn, c, 0, 0, status, s);
-  // decode rows are sequences [0, n_decode), one row each: rows [0, n_decode)
+  // decode rows are sequences [0, n_decode), one row each: rows [0, n_decode).
+  // With prefill rows too, both run in one persistent launch: the extend part
+  // on as many CTAs as make the two end together, the decode rows on the rest.
+  if (n_decode > 0 && total_q > n_decode && n_decode < n_seqs) {
+    cudaError_t ce;
+    if (persistent_ctas(&ce) >= 16) return run_extend(fn, c, n_decode, n_decode, status, s, n_decode);
+  }
   st = run_decode(fn, c, n_decode, true, status, s);
   if (st != CPE_OK) return st;
   return run_extend(fn, c, n_decode, n_decode, status, s);

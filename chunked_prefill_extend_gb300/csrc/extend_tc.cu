@@ -52,6 +52,7 @@
 // CPE_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
 // drained, TMEM is freed and the kernel returns.
 #include "cpe_device.cuh"
+#include "decode_item.cuh"
 #include "kernels.h"
 
 namespace cpe {
@@ -136,6 +137,30 @@ __device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, Item& it
   return true;
 }
 
+// Decode rows of a fused mixed step on a CTA the extend part does not use:
+// each of the CTA's three warpgroups takes decode items from the shared
+// counter and computes them as the stand-alone decode kernel's CTAs do, in its
+// own third of shared memory, on its own named barrier.
+template <int D>
+__device__ void decode_worker(const ExtendTcArgs& a, uint8_t* smem) {
+  static_assert(1024 + 3 * DecCfg<D>::kSmem + 64 <= TcCfg<D>::kSmem, "three decode items fit a CTA's shared memory");
+  const int wg = threadIdx.x / 128;
+  const int tid = threadIdx.x % 128;
+  uint8_t* dsm = smem + wg * DecCfg<D>::kSmem;
+  volatile int* slot = reinterpret_cast<volatile int*>(smem + 3 * DecCfg<D>::kSmem) + wg;
+  const int splits = a.dec.max_splits;
+  for (;;) {
+    if (tid == 0) *slot = atomicAdd(&a.sched.header[6], 1);
+    group_sync(1 + wg);
+    const int item = *slot;
+    group_sync(1 + wg);  // every thread has its item before the slot is reused
+    if (item >= a.dec_items) break;
+    const int sp = item % splits;
+    const int rest = item / splits;
+    decode_item<D>(a.dec, sp, rest / a.h_kv, rest % a.h_kv, dsm, tid, 1 + wg);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendTcArgs a) {
   using C = TcCfg<D>;
@@ -148,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int nc = a.sched.header[1];
   const int n_items = a.sched.header[3];  // item-table entries; CTA c takes c, c + nc, ...
   const int cta = blockIdx.x;
-  if (cta >= nc) return;  // CTAs without work (uniform over the CTA)
+  if (cta >= nc) {  // CTAs past the extend part: decode workers of a fused mixed step, else idle
+    if (a.dec_items > 0) decode_worker<D>(a, smem);
+    return;
+  }
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -790,6 +818,40 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs
   const int W = totals[0];
   const int n_max = totals[1];
   __syncthreads();
+  // fused mixed step: give the extend part the CTAs that make the two parts
+  // end together (decode time falls off below kDecodeSatSms reading SMs)
+  __shared__ int s_next;
+  if (a.dec_rows > 0) {
+    long long keys = 0;
+    for (int s = tid; s < a.dec_rows; s += blockDim.x) keys += a.prefix_len[s] + 1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) keys += __shfl_xor_sync(0xffffffffu, keys, o);
+    __shared__ long long dec_keys[32];
+    if ((tid & 31) == 0) dec_keys[tid >> 5] = keys;
+    __syncthreads();
+    if (tid == 0) {
+      long long tot = 0;
+      for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) tot += dec_keys[k];
+      const float t_dec = static_cast<float>(tot) * static_cast<float>(a.dec_bytes_per_key) / kDecodeBytesPerUs;
+      const float t_tile = kTileUsPerSm * kFusedExtendSlowdown * static_cast<float>(a.d) / 128.f;
+      int best_n = max(1, a.n_ctas - 1);
+      float best_t = 3.4e38f;
+      for (int nx = 4; nx <= a.n_ctas - 4; nx += 4) {
+        const float te = static_cast<float>(W) * t_tile / nx;
+        const float td = t_dec * fmaxf(1.f, static_cast<float>(kDecodeSatSms) / (a.n_ctas - nx));
+        if (fmaxf(te, td) < best_t) {
+          best_t = fmaxf(te, td);
+          best_n = nx;
+        }
+      }
+      s_next = best_n;
+    }
+    __syncthreads();
+  } else if (tid == 0) {
+    s_next = a.n_ctas;
+  }
+  __syncthreads();
+  const int n_ext = s_next;  // CTAs the extend part may use
   // 2. parts: items and partial slots each candidate S would need
   int v16[2 * kMaxParts] = {};
   for (int u = u_lo; u < u_hi; ++u) {
@@ -810,7 +872,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs
       const int T = max(1, (n_max + S - 1) / S);
       const int items = sums16[S - 1];
       if (S > 1 && (sums16[kMaxParts + S - 1] > a.max_slots || W < items * kMinTilesPerPart)) break;
-      const int ncp = max(1, min(a.n_ctas, items));
+      const int ncp = max(1, min(n_ext, items));
       const int waves = (items + ncp - 1) / ncp;
       const float eff = static_cast<float>(W) / (static_cast<float>(ncp) * T * waves);
       if (eff > best_eff + 0.03f) {  // more parts only when they fill the waves clearly better
@@ -863,7 +925,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs
   }
   __syncthreads();
   const int n_items = s_items;
-  const int nc = n_items > 0 ? min(a.n_ctas, n_items) : 0;
+  const int nc = n_items > 0 ? min(n_ext, n_items) : 0;
   const int table_len = nc > 0 ? (n_items + nc - 1) / nc * nc : 0;
   // the last wave's unused entries read as empty: its low CTAs' entries when
   // that wave runs backwards (odd), its high ones otherwise
@@ -898,6 +960,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs
     a.sched.header[3] = table_len;
     a.sched.header[4] = T;
     a.sched.header[5] = n_items;
+    a.sched.header[6] = 0;
   }
 }
 

@@ -37,13 +37,41 @@ struct UnitEntry {  // one extend work unit: two query tiles of one sequence and
 // c, c + header[1], ...
 struct ExtendSched {
   int* header;          // [0] total key tiles, [1] CTAs used, [2] units, [3] item table length
-                        // (a multiple of [1]), [4] target part length, [5] items
+                        // (a multiple of [1]), [4] target part length, [5] items, [6] next
+                        // decode item of a fused mixed step
   UnitEntry* units;     // [capacity]
   int* items;           // [item capacity]
   float* partial;       // slots: O [256 x d] (normalised), m [256] (log2), l [256]
 };
 
 __host__ __device__ constexpr size_t partial_slot_floats(int d) { return size_t(kUnitRows) * d + 2 * kUnitRows; }
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* page_table;
+  const int32_t* qo_indptr;   // nullable: row of sequence s is qo_indptr[s] (else s)
+  const int32_t* prefix_len;
+  void* out;
+  float* lse;
+  float* part_o;   // [n_seqs, h_q, max_splits, d] normalised partial outputs
+  float* part_ml;  // [n_seqs, h_q, max_splits, 2] (m in log2 units, l)
+  int* status;
+  int64_t num_pages;
+  int max_pages, n_seqs, seq_begin, h_q, h_kv, d, max_kv_len, max_splits;
+  float scale_log2;
+};
+
+// Rates that size the split of a fused mixed step between extend CTAs and
+// decode workers, measured on GB300 at d = 128: one key tile of a two-tile
+// unit takes one SM about 1.97 us alone and about 8 % longer beside decode
+// rows (they share HBM); decode rows stream K/V at about 55 GB/s per SM, which
+// reaches the 6.67 GB/ms the part sustains at about 120 SMs.
+constexpr float kTileUsPerSm = 1.97f;
+constexpr float kFusedExtendSlowdown = 1.08f;
+constexpr float kDecodeBytesPerUs = 6.67e6f;
+constexpr int kDecodeSatSms = 120;
 
 struct ScheduleArgs {
   const int32_t* qo_indptr;
@@ -58,6 +86,11 @@ struct ScheduleArgs {
   int max_slots;            // partial slots available
   ExtendSched sched;
   int* status;
+  // fused mixed step: decode rows [0, dec_rows) run on the CTAs the extend
+  // part leaves free (0: no decode rows in this launch)
+  int dec_rows;
+  int64_t dec_bytes_per_key;  // K + V bytes one key of one decode row reads
+  int d;
 };
 
 struct ExtendTcArgs {
@@ -77,6 +110,10 @@ struct ExtendTcArgs {
   uint64_t wait_ns;
   int n_ctas;
   int max_units;  // unit capacity (the merge kernel's grid)
+  // fused mixed step: CTAs past the extend part run these decode items
+  // ((sequence x KV head) x split, split fastest), taken from header[6]
+  DecodeArgs dec;
+  int dec_items;
 };
 
 struct ExtendSimtArgs {
@@ -108,28 +145,13 @@ struct KvAppendArgs {
   int max_pages, n_seqs, total_q, row_bytes, page_size;
 };
 
-struct DecodeArgs {
-  const void* q;
-  const void* k_cache;
-  const void* v_cache;
-  const int32_t* page_table;
-  const int32_t* qo_indptr;   // nullable: row of sequence s is qo_indptr[s] (else s)
-  const int32_t* prefix_len;
-  void* out;
-  float* lse;
-  float* part_o;   // [n_seqs, h_q, max_splits, d] normalised partial outputs
-  float* part_ml;  // [n_seqs, h_q, max_splits, 2] (m in log2 units, l)
-  int* status;
-  int64_t num_pages;
-  int max_pages, n_seqs, seq_begin, h_q, h_kv, d, max_kv_len, max_splits;
-  float scale_log2;
-};
 
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s);
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s);  // + the merge of split units
 cudaError_t launch_extend_simt(const ExtendSimtArgs& a, cudaStream_t s);
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t s);  // combine the splits of decode rows
 size_t extend_tc_smem_bytes(int d);
 
 }  // namespace cpe

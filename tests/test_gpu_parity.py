@@ -225,6 +225,24 @@ def test_mixed_step_small_full(cpe):
     np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 
+@pytest.mark.parametrize("h_q,h_kv,d", [(8, 1, 64), (32, 2, 128)])
+def test_mixed_step_fused_shapes_full(cpe, h_q, h_kv, d):
+    """Decode rows (one past a split boundary) and two prefill chunks in one
+    fused launch, at d = 64 and G = 16; every row checked."""
+    ctx = [3, 2049, 4100, 77]
+    plan = cpe.cpe_plan_schedule(4 + 300, [(L - 1, 1) for L in ctx] + [(900, 200)], [(64, 300)])
+    lens = [(p, plan["qo_indptr"][i + 1] - plan["qo_indptr"][i]) for i, p in enumerate(plan["prefix_len"])]
+    b = varlen_batch(51, lens, h_q, h_kv, d)
+    lse = torch.empty(b["q"].shape[0], h_q, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(b["q"], b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"],
+                                i32(b["qo"]), i32(b["pl"]), plan["n_decode"], b["max_kv"], lse=lse)
+    _status_ok(cpe)
+    kc, vc = b["k_cache"].cpu().clone(), b["v_cache"].cpu().clone()
+    ref_o, ref_l = oracle.extend_attention(b["q"].cpu(), kc, vc, b["page_table_host"], b["qo"], b["pl"], h_q, h_kv)
+    check_close(out, ref_o, f"fused mixed {h_q}/{h_kv} d={d}")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
 def test_cfg4_mixed_sampled(cpe):
     spec = W.CONFIGS["cfg4"]
     g = torch.Generator().manual_seed(spec.seed)
