@@ -100,6 +100,15 @@ class Chunked:
         self.bound = "tensor"
         self.small = self.in_bytes + 2 * self.req.k_cache.numel() * self.req.k_cache.element_size() < 2 * L2_BYTES
 
+    def chunk_call(self, c, q, k, v, out):
+        """One round: its K/V appended and its extend attention, in one call
+        (cpe_mixed_step with no decode rows)."""
+        qo, pl = self.idx[c.index]
+        a = c.prefix_len - self.cached
+        self.cpe.cpe_mixed_step(q[a:a + c.query_len], k[a:a + c.query_len], v[a:a + c.query_len], self.req.k_cache,
+                                self.req.v_cache, self.req.page_table, qo, pl, 0, c.seq_len,
+                                out=out[a:a + c.query_len], workspace=self.ws)
+
     def step(self, ev=None, q=None, k=None, v=None, out=None):
         cpe, req = self.cpe, self.req
         q = req.q if q is None else q
@@ -108,15 +117,10 @@ class Chunked:
         out = self.out if out is None else out
         chunks, _, _ = cpe.cpe_plan_chunks(self.spec.input_len, self.spec.hit_rate, self.spec.chunk)
         for c in chunks[self.rounds[0]:self.rounds[1]]:
-            qo, pl = self.idx[c.index]
-            a = c.prefix_len - self.cached
-            cpe.cpe_kv_append(k[a:a + c.query_len], v[a:a + c.query_len], req.k_cache, req.v_cache,
-                              req.page_table, qo, pl)
             if ev is not None:
                 ev[0].append(torch.cuda.Event(enable_timing=True))
                 ev[0][-1].record()
-            cpe.cpe_extend_attention(q[a:a + c.query_len], req.k_cache, req.v_cache, req.page_table, qo, pl,
-                                     c.seq_len, out=out[a:a + c.query_len], workspace=self.ws)
+            self.chunk_call(c, q, k, v, out)
             if ev is not None:
                 ev[1].append(torch.cuda.Event(enable_timing=True))
                 ev[1][-1].record()
@@ -147,12 +151,7 @@ class Chunked:
         q, k, v = dev_in
         for c, e in zip(chunks, ev_in):
             main.wait_event(e)
-            qo, pl = self.idx[c.index]
-            a = c.prefix_len - self.cached
-            cpe.cpe_kv_append(k[a:a + c.query_len], v[a:a + c.query_len], req.k_cache, req.v_cache,
-                              req.page_table, qo, pl)
-            cpe.cpe_extend_attention(q[a:a + c.query_len], req.k_cache, req.v_cache, req.page_table, qo, pl,
-                                     c.seq_len, out=dev_out[a:a + c.query_len], workspace=self.ws)
+            self.chunk_call(c, q, k, v, dev_out)
             e2 = torch.cuda.Event()
             e2.record(main)
             ev_out.append(e2)
@@ -536,7 +535,8 @@ def run_ours(args, ws, rank, local):
         traffic = (profiled_traffic(per_launch)
                    if args.workload == "cfg5" and not args.input_len and not args.rounds else None)
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
-                "traffic": traffic, "kernel": "extend attention call (schedule_kernel + extend_tc_kernel)",
+                "traffic": traffic,
+                "kernel": "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)",
                 "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": per_launch}
         last = kms_list[-len(wl.chunks):]
         curve = [(c.prefix_len, chunk_flops(wl.spec.d, wl.spec.h_q, c.prefix_len, c.query_len) / (t * 1e-3) / 1e12)

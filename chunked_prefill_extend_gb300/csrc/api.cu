@@ -198,9 +198,10 @@ DecodeArgs decode_args(const Common& c, const Layout& L, int n_dec, bool use_qo,
 
 // Extend path over sequences [seq_begin, n_seqs), whose rows are [row_begin, total_q).
 // With dec_rows > 0 (a mixed step, bf16) the decode rows [0, dec_rows) run in the
-// same persistent launch on the CTAs the extend part leaves free.
+// same persistent launch on the CTAs the extend part leaves free; with `append`
+// the round's K/V append shares the schedule's launch.
 cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_begin, int* status,
-                      cudaStream_t stream, int dec_rows = 0) {
+                      cudaStream_t stream, int dec_rows = 0, const KvAppendArgs* append = nullptr) {
   if (c.total_q - row_begin <= 0 || seq_begin >= c.n_seqs) return CPE_OK;
   const Layout L = workspace_layout(c.n_seqs, c.total_q, c.h_q, c.h_kv, c.d, c.max_kv_len);
   cudaError_t e;
@@ -235,7 +236,7 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   sa.d = c.d;
   sa.dec_rows = dec_rows;
   sa.dec_bytes_per_key = static_cast<int64_t>(c.h_kv) * c.d * 2 * 2;
-  e = launch_schedule(sa, stream);
+  e = append ? launch_prep(sa, *append, stream) : launch_schedule(sa, stream);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 1;
 
@@ -258,7 +259,9 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
     a.dec = decode_args(c, L, dec_rows, true, status);
     a.dec_items = dec_rows * c.h_kv * L.max_splits;
   }
-  e = launch_extend_tc(a, stream);
+  // dependent launches hide launch latency; worth it only on short launches
+  const double flops_bound = 4.0 * c.d * c.h_q * static_cast<double>(n_rows) * c.max_kv_len;
+  e = launch_extend_tc(a, stream, flops_bound < kDependentLaunchFlops);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 2;  // the extend kernel and the merge of key-range parts
   if (dec_rows > 0 && L.max_splits > 1) {
@@ -396,23 +399,32 @@ cpe_status cpe_mixed_step(const void* q, const void* k_new, const void* v_new, v
   if (n_decode < 0 || n_decode > n_seqs || n_decode > total_q)
     return fail(CPE_ERR_INVALID_ARG, fn, "n_decode must be in [0, min(n_seqs, total_q)]");
   if (!k_new || !v_new) return fail(CPE_ERR_INVALID_ARG, fn, "null k_new / v_new");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(CPE_ERR_INVALID_ARG, fn, "misaligned k_new / v_new");
   if (total_q == 0) return CPE_OK;
-  st = cpe_kv_append(k_new, v_new, k_cache, v_cache, num_pages, page_table, max_pages, qo_indptr, prefix_len, n_seqs,
-                     total_q, h_kv, d, page_size, dtype, stream);
-  if (st != CPE_OK) return st;
   cudaError_t e;
   int* status = status_ptr(&e);
   if (!status) return cuda_fail(fn, e);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // bf16 with prefill rows: the append rides in the extend schedule's launch
+  if (dtype == CPE_BF16 && total_q > n_decode && n_decode < n_seqs) {
+    KvAppendArgs ka{};
+    ka.k_new = k_new; ka.v_new = v_new; ka.k_cache = k_cache; ka.v_cache = v_cache; ka.page_table = page_table;
+    ka.qo_indptr = qo_indptr; ka.prefix_len = prefix_len; ka.status = status; ka.num_pages = num_pages;
+    ka.max_pages = max_pages; ka.n_seqs = n_seqs; ka.total_q = total_q; ka.row_bytes = h_kv * d * 2;
+    ka.page_size = page_size;
+    // (nothing may read the cache before the prep launch: no decode rows, or
+    // decode rows inside the same fused launch)
+    cudaError_t ce;
+    if (n_decode == 0) return run_extend(fn, c, 0, 0, status, s, 0, &ka);
+    if (persistent_ctas(&ce) >= 16) return run_extend(fn, c, n_decode, n_decode, status, s, n_decode, &ka);
+  }
+  st = cpe_kv_append(k_new, v_new, k_cache, v_cache, num_pages, page_table, max_pages, qo_indptr, prefix_len, n_seqs,
+                     total_q, h_kv, d, page_size, dtype, stream);
+  if (st != CPE_OK) return st;
   // fp32 data: the CUDA-core path computes every row, decode rows included
   if (dtype == CPE_F32) return run_extend(fn, c, 0, 0, status, s);
-  // decode rows are sequences [0, n_decode), one row each: rows [0, n_decode).
-  // With prefill rows too, both run in one persistent launch: the extend part
-  // on as many CTAs as make the two end together, the decode rows on the rest.
-  if (n_decode > 0 && total_q > n_decode && n_decode < n_seqs) {
-    cudaError_t ce;
-    if (persistent_ctas(&ce) >= 16) return run_extend(fn, c, n_decode, n_decode, status, s, n_decode);
-  }
+  // decode rows only (or too few SMs to share): decode rows are sequences
+  // [0, n_decode), one row each (rows [0, n_decode)), then the extend path
   st = run_decode(fn, c, n_decode, true, status, s);
   if (st != CPE_OK) return st;
   return run_extend(fn, c, n_decode, n_decode, status, s);

@@ -53,6 +53,7 @@
 // drained, TMEM is freed and the kernel returns.
 #include "cpe_device.cuh"
 #include "decode_item.cuh"
+#include "kv_append_row.cuh"
 #include "kernels.h"
 
 namespace cpe {
@@ -170,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars<NK, NV>* bars = reinterpret_cast<Bars<NK, NV>*>(smem + C::kBarOff);
 
+  grid_dependency_wait();    // the schedule (and the round's K/V append) are complete
+  grid_launch_dependents();  // the merge kernels may be scheduled as CTAs finish
   const int nc = a.sched.header[1];
   const int n_items = a.sched.header[3];  // item-table entries; CTA c takes c, c + nc, ...
   const int cta = blockIdx.x;
@@ -586,6 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 // unit's rows.  Block b takes unit b; 256 threads, one row each.
 template <int D>
 __global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant__ ExtendTcArgs a) {
+  grid_dependency_wait();  // the extend launch's partials are complete
+  grid_launch_dependents();
   const int n_units = a.sched.header[2];
   const int u = blockIdx.x;
   if (u >= n_units) return;
@@ -740,7 +745,7 @@ __device__ void block_scan_n(int (&v)[N], int (*scratch)[N], int* totals) {
 //    same key range of a KV head).  Position k of that order goes to CTA
 //    k mod nc in even waves and nc - 1 - k mod nc in odd ones (snake order),
 //    which evens out the CTAs' totals.
-__global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs a) {
+__device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   constexpr int kRuns = kMaxParts * kSizeBuckets;  // (part, size class) counters
   __shared__ int warp_sums[32];
   __shared__ int scratch[32][kRuns];
@@ -964,6 +969,23 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs
   }
 }
 
+__global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs a) {
+  grid_launch_dependents();  // the extend launch may be scheduled (it waits for this one)
+  schedule_body(a);
+}
+
+// A mixed step's prep launch: block 0 builds the extend schedule while the
+// other blocks append the round's K/V rows (kAppendRowsPerBlock per block); the
+// schedule reads only the index arrays, so the two are independent.
+static_assert(kSchedThreads == kAppendRowsPerBlock * 32, "one warp per appended row");
+__global__ void __launch_bounds__(kSchedThreads) prep_kernel(ScheduleArgs a, KvAppendArgs k) {
+  grid_launch_dependents();
+  if (blockIdx.x == 0)
+    schedule_body(a);
+  else
+    append_row(k, (blockIdx.x - 1) * kAppendRowsPerBlock + (threadIdx.x >> 5), threadIdx.x & 31);
+}
+
 }  // namespace
 
 size_t extend_tc_smem_bytes(int d) {
@@ -972,6 +994,12 @@ size_t extend_tc_smem_bytes(int d) {
 
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
   schedule_kernel<<<1, kSchedThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream_t s) {
+  const int blocks = 1 + (k.total_q + kAppendRowsPerBlock - 1) / kAppendRowsPerBlock;
+  prep_kernel<<<blocks, kSchedThreads, 0, s>>>(a, k);
   return cudaGetLastError();
 }
 
@@ -985,7 +1013,26 @@ cudaError_t check_regs() {
   return fa.numRegs >= kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
-cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s) {
+// Launch, with programmatic stream serialisation if `dependent`: the kernel may
+// then be scheduled while the one before it finishes and waits in
+// grid_dependency_wait().
+template <typename Kernel, typename Arg>
+cudaError_t launch_dependent(Kernel kernel, int grid, int block, int smem, cudaStream_t s, const Arg& arg,
+                             bool dependent) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
+cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
   if (a.n_ctas <= 0) return cudaSuccess;
   cudaError_t ce = a.d == 128 ? check_regs<128>() : check_regs<64>();
   if (ce != cudaSuccess) return ce;
@@ -993,18 +1040,18 @@ cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s) {
     const int smem = TcCfg<128>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    extend_tc_kernel<128><<<a.n_ctas, kThreads, smem, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, smem, s, a, dependent);
     if (e != cudaSuccess) return e;
-    extend_merge_kernel<128><<<a.max_units, 256, 0, s>>>(a);
+    e = launch_dependent(extend_merge_kernel<128>, a.max_units, 256, 0, s, a, dependent);
+    if (e != cudaSuccess) return e;
   } else {
     const int smem = TcCfg<64>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    extend_tc_kernel<64><<<a.n_ctas, kThreads, smem, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, smem, s, a, dependent);
     if (e != cudaSuccess) return e;
-    extend_merge_kernel<64><<<a.max_units, 256, 0, s>>>(a);
+    e = launch_dependent(extend_merge_kernel<64>, a.max_units, 256, 0, s, a, dependent);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

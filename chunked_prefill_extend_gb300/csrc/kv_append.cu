@@ -1,61 +1,21 @@
-// KV append: write the round's new K/V rows into their page slots.
-// One warp per new row; a row's [H_kv, d] block is contiguous on both sides,
-// so the copy is whole 16-byte vectors, coalesced on the read and the write.
-#include "cpe_device.cuh"
-#include "kernels.h"
+// The stand-alone KV append kernel (append_row of kv_append_row.cuh, one
+// warp per row).
+#include "kv_append_row.cuh"
 
 namespace cpe {
 
 namespace {
 
-__device__ __forceinline__ int seq_of_row(const int32_t* qo_indptr, int n_seqs, int row) {
-  int lo = 0, hi = n_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (qo_indptr[mid] <= row) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendArgs a) {
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (row >= a.total_q) return;
-  const int s = seq_of_row(a.qo_indptr, a.n_seqs, row);
-  const int pos = a.prefix_len[s] + row - a.qo_indptr[s];
-  const int pidx = pos / a.page_size;
-  if (pos < 0 || pidx >= a.max_pages) {
-    if (lane == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
-    return;
-  }
-  const int pid = a.page_table[static_cast<int64_t>(s) * a.max_pages + pidx];
-  if (pid < 0 || pid >= a.num_pages) {
-    if (lane == 0) record_error(a.status, kStatusDeviceArg, kDetailBadPage);
-    return;
-  }
-  const int64_t dst = (static_cast<int64_t>(pid) * a.page_size + pos % a.page_size) * a.row_bytes;
-  const int64_t src = static_cast<int64_t>(row) * a.row_bytes;
-  const int nvec = a.row_bytes >> 4;
-  const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k_new) + src);
-  const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.v_new) + src);
-  uint4* kd = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.k_cache) + dst);
-  uint4* vd = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.v_cache) + dst);
-  for (int x = lane; x < nvec; x += 32) {
-    const uint4 kv = __ldg(ks + x);
-    const uint4 vv = __ldg(vs + x);
-    kd[x] = kv;
-    vd[x] = vv;
-  }
+  append_row(a, blockIdx.x * kAppendRowsPerBlock + (threadIdx.x >> 5), threadIdx.x & 31);
 }
 
 }  // namespace
 
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t s) {
   if (a.total_q <= 0) return cudaSuccess;
-  const int rows_per_block = 8;
-  const int blocks = (a.total_q + rows_per_block - 1) / rows_per_block;
-  kv_append_kernel<<<blocks, rows_per_block * 32, 0, s>>>(a);
+  const int blocks = (a.total_q + kAppendRowsPerBlock - 1) / kAppendRowsPerBlock;
+  kv_append_kernel<<<blocks, kAppendRowsPerBlock * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 

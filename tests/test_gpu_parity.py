@@ -113,15 +113,20 @@ def test_page_permutation_gives_bitwise_equal_output(cpe):
 
 # ---------------------------------------------------------------- chunked == one-shot
 
-def _chunked_run(cpe, spec, device="cuda"):
+def _chunked_run(cpe, spec, device="cuda", one_call=False):
+    """Every round through cpe_kv_append + cpe_extend_attention, or (one_call)
+    through cpe_mixed_step with no decode rows (append and schedule share a launch)."""
     req = W.make_chunked(spec, device=device)
     chunks, _, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
     outs = []
     for ch in chunks:
         q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
         qo, pl = i32([0, ch.query_len]), i32([ch.prefix_len])
-        cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, qo, pl)
-        out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, qo, pl, ch.seq_len)
+        if one_call:
+            out, _ = cpe.cpe_mixed_step(q, k, v, req.k_cache, req.v_cache, req.page_table, qo, pl, 0, ch.seq_len)
+        else:
+            cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, qo, pl)
+            out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, qo, pl, ch.seq_len)
         outs.append(out)
     _status_ok(cpe)
     return req, chunks, torch.cat(outs)
@@ -146,13 +151,18 @@ def test_bf16_chunked_equals_one_shot(cpe):
     check_close(out, one, "bf16 chunked vs one-shot")
     _, _, out1 = _chunked_run(cpe, W.shrink(spec, chunk=1500))
     check_close(out, out1.double().cpu().numpy(), "bf16 gpu chunked vs gpu one-shot")
+    # one call per round (append inside the extend schedule's launch): same rounds, same answer
+    _, _, out2 = _chunked_run(cpe, spec, one_call=True)
+    check_close(out2, one, "bf16 chunked one call per round vs one-shot")
+    assert torch.equal(out2, out)
 
 
 # ---------------------------------------------------------------- full-size workloads
 
 def test_cfg2_full(cpe):
+    """Every row of cfg2, each round in one call as the benchmark runs it."""
     spec = W.CONFIGS["cfg2"]
-    req, chunks, out = _chunked_run(cpe, spec)
+    req, chunks, out = _chunked_run(cpe, spec, one_call=True)
     assert [c.query_len for c in chunks] == [512] * 7 + [416]
     one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
     check_close(out, one, "cfg2 all rows")
