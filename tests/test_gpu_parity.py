@@ -157,6 +157,49 @@ def test_bf16_chunked_equals_one_shot(cpe):
     assert torch.equal(out2, out)
 
 
+def test_shared_prefix_pages_with_aligned_first_cut(cpe):
+    """Radix-style sharing: two requests whose cached prefixes are the same 62
+    full pages (992 tokens) in the page pool; each is chunked with the first cut
+    aligned to the page size, and their rounds run together as one varlen
+    batch.  Every round matches the oracle and the shared pages are never
+    written."""
+    h_q, h_kv, d, pg = 32, 8, 128, 16
+    plans = [cpe.cpe_plan_chunks(3968, 0.25, 500, align_to=pg)[0], cpe.cpe_plan_chunks(1984, 0.5, 500, align_to=pg)[0]]
+    assert [c.prefix_len for c in plans[0]][:2] == [992, 1488] and plans[0][0].query_len == 496
+    g = torch.Generator().manual_seed(81)
+    shared = 992 // pg
+    own = [-(-3968 // pg) - shared, -(-1984 // pg) - shared]
+    n_pages = shared + sum(own) + 2
+    perm = torch.randperm(n_pages, generator=g).to(torch.int32)
+    pt = torch.full((2, shared + max(own)), -1, dtype=torch.int32)
+    pt[:, :shared] = perm[:shared]  # the same physical pages for both prefixes
+    pt[0, shared:shared + own[0]] = perm[shared:shared + own[0]]
+    pt[1, shared:shared + own[1]] = perm[shared + own[0]:shared + own[0] + own[1]]
+    kc = (torch.randn(n_pages, pg, h_kv, d, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    vc = (torch.randn(n_pages, pg, h_kv, d, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    ptd = pt.cuda()
+    shared_ids = pt[0, :shared].long().cuda()
+    k_shared, v_shared = kc[shared_ids].clone(), vc[shared_ids].clone()
+    for t in range(max(len(p) for p in plans)):
+        seqs = [r for r in range(2) if t < len(plans[r])]
+        lens = [(plans[r][t].prefix_len, plans[r][t].query_len) for r in seqs]
+        rows = sum(E for _, E in lens)
+        q = (torch.randn(rows, h_q, d, generator=g) * 0.5).to(torch.bfloat16).cuda()
+        kn = (torch.randn(rows, h_kv, d, generator=g) * 0.5).to(torch.bfloat16).cuda()
+        vn = (torch.randn(rows, h_kv, d, generator=g) * 0.5).to(torch.bfloat16).cuda()
+        qo = [0]
+        for _, E in lens:
+            qo.append(qo[-1] + E)
+        sub = ptd[seqs].contiguous()
+        out, _ = cpe.cpe_mixed_step(q, kn, vn, kc, vc, sub, i32(qo), i32([P for P, _ in lens]), 0,
+                                    max(P + E for P, E in lens))
+        _status_ok(cpe)
+        ref_o, _ = oracle.extend_attention(q.cpu(), kc.cpu(), vc.cpu(), pt[seqs].contiguous(), qo,
+                                           [P for P, _ in lens], h_q, h_kv)
+        check_close(out, ref_o, f"shared-prefix round {t}")
+    assert torch.equal(kc[shared_ids], k_shared) and torch.equal(vc[shared_ids], v_shared)
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def test_cfg2_full(cpe):
