@@ -538,11 +538,15 @@ def run_ours(args, ws, rank, local):
                 "traffic": traffic,
                 "kernel": "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)",
                 "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": per_launch}
-        last = kms_list[-len(wl.chunks):]
+        # per round: the median over the timed steps of that round's call
+        nch = len(wl.chunks)
+        med = [statistics.median(kms_list[i::nch]) for i in range(nch)]
         curve = [(c.prefix_len, chunk_flops(wl.spec.d, wl.spec.h_q, c.prefix_len, c.query_len) / (t * 1e-3) / 1e12)
-                 for c, t in zip(wl.chunks, last)]
+                 for c, t in zip(wl.chunks, med)]
         pick = sorted(set([0, len(curve) // 4, len(curve) // 2, 3 * len(curve) // 4, len(curve) - 1]))
         roof["per_chunk_tflops"] = {str(curve[i][0]): round(curve[i][1], 1) for i in pick}
+        roof["per_chunk_reps"] = len(kms_list) // nch
+        roof["aggregate_tflops"] = wl.flops / (sum(med) * 1e-3) / 1e12  # sum of flops / sum of median times
 
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else e2e_measure(wl, args, device, ws)

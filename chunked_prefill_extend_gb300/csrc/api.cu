@@ -108,7 +108,7 @@ Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int m
   L.partial_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(int));
   L.slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
   const size_t parts = static_cast<size_t>(n_seqs) * h_q * L.max_splits;
-  L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_floats(d) * sizeof(float));
+  L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_bytes(d));
   L.part_ml_off = L.part_o_off + align256(parts * d * sizeof(float));
   L.total = L.part_ml_off + align256(parts * 2 * sizeof(float));
   return L;
@@ -120,7 +120,7 @@ ExtendSched sched_of(const Layout& L, void* ws) {
   s.header = reinterpret_cast<int*>(b + L.header_off);
   s.units = reinterpret_cast<UnitEntry*>(b + L.units_off);
   s.items = reinterpret_cast<int*>(b + L.items_off);
-  s.partial = reinterpret_cast<float*>(b + L.partial_off);
+  s.partial = b + L.partial_off;
   return s;
 }
 

@@ -407,7 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const uint32_t s_col = t * 128;
     const uint32_t o_col = 256 + t * D;
     const float sl2 = a.scale_log2;
-    const size_t slot_floats = partial_slot_floats(D);
     int sc = 0, od = 0;
     bool ok = true;
     Item it;
@@ -420,11 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const int R = t * kBlockM + r;               // row of the unit
       if (it.kv_lo >= jhi) {
         // no key tile of this portion reaches this query tile: an empty partial
-        if (!it.whole) {
-          float* part = a.sched.partial + static_cast<size_t>(it.slot) * slot_floats;
-          for (int c = 0; c < D; ++c) part[static_cast<size_t>(R) * D + c] = 0.f;
-          part[static_cast<size_t>(kUnitRows) * D + R] = -INFINITY;
-          part[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] = 0.f;
+        if (!it.whole) {  // l = 0 tells the merge to skip this part's O
+          float* ml = reinterpret_cast<float*>(a.sched.partial + static_cast<size_t>(it.slot) * partial_slot_bytes(D) +
+                                               static_cast<size_t>(kUnitRows) * D * 2);
+          ml[R] = -INFINITY;
+          ml[kUnitRows + R] = 0.f;
         }
         continue;
       }
@@ -559,20 +558,24 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           a.lse[static_cast<int64_t>(it.q0 + i) * a.h_q + head] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       } else {
         // one part of a unit: the normalised partial goes to the item's slot
-        float* part = a.sched.partial + static_cast<size_t>(it.slot) * slot_floats;
-        float4* prow = reinterpret_cast<float4*>(part + static_cast<size_t>(R) * D);
+        uint8_t* slot = a.sched.partial + static_cast<size_t>(it.slot) * partial_slot_bytes(D);
+        uint4* prow = reinterpret_cast<uint4*>(slot + static_cast<size_t>(R) * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t raw[32];
           tmem_ld32(tmem + lane_base + o_col + c * 32, raw);
           tc_wait_ld_dep(raw);
 #pragma unroll
-          for (int x = 0; x < 8; ++x)
-            prow[c * 8 + x] = make_float4(__uint_as_float(raw[4 * x]) * inv_l, __uint_as_float(raw[4 * x + 1]) * inv_l,
-                                          __uint_as_float(raw[4 * x + 2]) * inv_l, __uint_as_float(raw[4 * x + 3]) * inv_l);
+          for (int x = 0; x < 4; ++x)  // 32 columns = four 16-byte vectors of bf16 pairs
+            prow[c * 4 + x] = make_uint4(
+                pack_bf16x2(__uint_as_float(raw[8 * x + 0]) * inv_l, __uint_as_float(raw[8 * x + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(raw[8 * x + 2]) * inv_l, __uint_as_float(raw[8 * x + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(raw[8 * x + 4]) * inv_l, __uint_as_float(raw[8 * x + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(raw[8 * x + 6]) * inv_l, __uint_as_float(raw[8 * x + 7]) * inv_l));
         }
-        part[static_cast<size_t>(kUnitRows) * D + R] = m_run;
-        part[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] = l_run;
+        float* ml = reinterpret_cast<float*>(slot + static_cast<size_t>(kUnitRows) * D * 2);
+        ml[R] = m_run;
+        ml[kUnitRows + R] = l_run;
       }
     }
   }
@@ -605,31 +608,33 @@ __global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant
   const int E = a.qo_indptr[e.seq + 1] - q0;
   const int i = (2 * e.pair + t) * a.tok + r / a.group;
   if (i >= E) return;
-  const size_t slot_floats = partial_slot_floats(D);
+  auto slot_of = [&](int p) { return a.sched.partial + static_cast<size_t>(e.slot + p) * partial_slot_bytes(D); };
+  auto ml_of = [&](int p) { return reinterpret_cast<const float*>(slot_of(p) + static_cast<size_t>(kUnitRows) * D * 2); };
   float M = -INFINITY;
   for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
-    const float* sl = a.sched.partial + static_cast<size_t>(e.slot + p) * slot_floats;
-    if (sl[static_cast<size_t>(kUnitRows) * D + kUnitRows + R] > 0.f)
-      M = fmaxf(M, sl[static_cast<size_t>(kUnitRows) * D + R]);
+    const float* ml = ml_of(p);
+    if (ml[kUnitRows + R] > 0.f) M = fmaxf(M, ml[R]);
   }
   float wsum = 0.f;
   float o[D];
 #pragma unroll
   for (int d = 0; d < D; ++d) o[d] = 0.f;
   for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
-    const float* sl = a.sched.partial + static_cast<size_t>(e.slot + p) * slot_floats;
-    const float l = sl[static_cast<size_t>(kUnitRows) * D + kUnitRows + R];
+    const float* ml = ml_of(p);
+    const float l = ml[kUnitRows + R];
     if (!(l > 0.f)) continue;  // this part holds no key of this row
-    const float w = fast_exp2(sl[static_cast<size_t>(kUnitRows) * D + R] - M) * l;
+    const float w = fast_exp2(ml[R] - M) * l;
     wsum += w;
-    const float4* row = reinterpret_cast<const float4*>(sl + static_cast<size_t>(R) * D);
+    const uint4* row = reinterpret_cast<const uint4*>(slot_of(p) + static_cast<size_t>(R) * D * 2);
 #pragma unroll
-    for (int d4 = 0; d4 < D / 4; ++d4) {
-      const float4 v = row[d4];
-      o[4 * d4] += w * v.x;
-      o[4 * d4 + 1] += w * v.y;
-      o[4 * d4 + 2] += w * v.z;
-      o[4 * d4 + 3] += w * v.w;
+    for (int d8 = 0; d8 < D / 8; ++d8) {  // eight bf16 per vector; bf16 -> fp32 is a shift
+      const uint4 v = row[d8];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        o[8 * d8 + 2 * k] += w * __uint_as_float(u[k] << 16);
+        o[8 * d8 + 2 * k + 1] += w * __uint_as_float(u[k] & 0xffff0000u);
+      }
     }
   }
   const float inv = 1.f / wsum;

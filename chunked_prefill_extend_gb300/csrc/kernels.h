@@ -41,10 +41,13 @@ struct ExtendSched {
                         // decode item of a fused mixed step
   UnitEntry* units;     // [capacity]
   int* items;           // [item capacity]
-  float* partial;       // slots: O [256 x d] (normalised), m [256] (log2), l [256]
+  uint8_t* partial;     // slots of partial_slot_bytes(d): O [256 x d] bf16 (normalised), then m [256]
+                        // (log2) and l [256] fp32
 };
 
-__host__ __device__ constexpr size_t partial_slot_floats(int d) { return size_t(kUnitRows) * d + 2 * kUnitRows; }
+__host__ __device__ constexpr size_t partial_slot_bytes(int d) {
+  return size_t(kUnitRows) * d * 2 + 2 * size_t(kUnitRows) * 4;
+}
 
 struct DecodeArgs {
   const void* q;
