@@ -200,6 +200,25 @@ def test_shared_prefix_pages_with_aligned_first_cut(cpe):
     assert torch.equal(kc[shared_ids], k_shared) and torch.equal(vc[shared_ids], v_shared)
 
 
+def test_many_short_sequences(cpe):
+    """2100 short sequences (over the schedule's 2048-sequence and 8192-unit
+    shared-memory caches, so both fall back to global memory) in one extend
+    call; the first and last row of every sequence and 600 more rows checked."""
+    g = torch.Generator().manual_seed(91)
+    n = 2100
+    E = torch.randint(1, 41, (n,), generator=g).tolist()
+    P = torch.randint(0, 201, (n,), generator=g).tolist()
+    b = varlen_batch(92, list(zip(P, E)), 32, 8, 128, spare_pages=0)
+    out, lse = _append_and_attend(cpe, b)
+    qo = b["qo"]
+    rows = sorted(set([qo[s] for s in range(n)] + [qo[s + 1] - 1 for s in range(n)] +
+                      torch.randint(0, qo[-1], (600,), generator=g).tolist()))
+    kc, vc = b["k_cache"].cpu().clone(), b["v_cache"].cpu().clone()
+    ref_o, ref_l = oracle.extend_attention(b["q"].cpu(), kc, vc, b["page_table_host"], qo, b["pl"], 32, 8, rows=rows)
+    check_close(out[rows], ref_o, "many short sequences")
+    np.testing.assert_allclose(lse[rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def test_cfg2_full(cpe):
