@@ -521,7 +521,7 @@ def run_ours(args, ws, rank, local):
         achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                "kernel": "mixed-step call (schedule_kernel + extend_tc_kernel with decode workers + merges)",
+                "kernel": "mixed-step call (prep_kernel: schedule + K/V append; extend_tc_kernel with decode workers; merges)",
                 "peak_source": peaks["source"] + " hbm_gbs", "units_per_launch": step_bytes,
                 "decode_kernel_alone": {"achieved": wl.decode_bytes / (dms * 1e-3) / 1e9, "unit": "GB/s",
                                         "frac": wl.decode_bytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"],
