@@ -93,6 +93,7 @@ class Chunked:
                               torch.tensor([c.prefix_len], dtype=torch.int32, device=device)) for c in self.chunks}
         self.out = torch.empty_like(self.req.q)
         self.ws = cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, device)
+        self.views = {}
         self.flops = sum(chunk_flops(spec.d, spec.h_q, c.prefix_len, c.query_len) for c in self.chunks)
         self.tokens = sum(c.query_len for c in self.chunks)
         self.in_bytes = sum(t.numel() * t.element_size() for t in (self.req.q, self.req.k, self.req.v))
@@ -102,12 +103,16 @@ class Chunked:
 
     def chunk_call(self, c, q, k, v, out):
         """One round: its K/V appended and its extend attention, in one call
-        (cpe_mixed_step with no decode rows)."""
+        (cpe_mixed_step with no decode rows).  The round's row views of the
+        request buffers are made once and reused."""
+        key = (c.index, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr())
+        views = self.views.get(key)
+        if views is None:
+            a = c.prefix_len - self.cached
+            views = self.views[key] = tuple(t[a:a + c.query_len] for t in (q, k, v, out))
         qo, pl = self.idx[c.index]
-        a = c.prefix_len - self.cached
-        self.cpe.cpe_mixed_step(q[a:a + c.query_len], k[a:a + c.query_len], v[a:a + c.query_len], self.req.k_cache,
-                                self.req.v_cache, self.req.page_table, qo, pl, 0, c.seq_len,
-                                out=out[a:a + c.query_len], workspace=self.ws)
+        self.cpe.cpe_mixed_step(views[0], views[1], views[2], self.req.k_cache, self.req.v_cache, self.req.page_table,
+                                qo, pl, 0, c.seq_len, out=views[3], workspace=self.ws)
 
     def step(self, ev=None, q=None, k=None, v=None, out=None):
         cpe, req = self.cpe, self.req

@@ -95,7 +95,7 @@ def _check(st: int, where: str):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -106,10 +106,16 @@ def _dtype(t: torch.Tensor) -> int:
     raise TypeError(f"libcpe takes bfloat16 or float32 tensors, got {t.dtype}")
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    """The stream handle: the given stream's, else the current device's current stream."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 @dataclass(frozen=True)

@@ -81,6 +81,37 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+// make_map through a small per-thread cache of encoded maps: successive calls
+// on the same cache reuse its four maps (only the query map follows the chunk).
+bool cached_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_heads, int box_rows) {
+  struct Entry {
+    CUtensorMap map;
+    const void* base;
+    int64_t rows;
+    int d, heads, box_heads, box_rows;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (const Entry& e : cache)
+    if (e.base == base && base != nullptr && e.rows == rows && e.d == d && e.heads == heads &&
+        e.box_heads == box_heads && e.box_rows == box_rows) {
+      *m = e.map;
+      return true;
+    }
+  if (!make_map(m, base, d, heads, rows, box_heads, box_rows)) return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.map = *m;
+  e.base = base;
+  e.rows = rows;
+  e.d = d;
+  e.heads = heads;
+  e.box_heads = box_heads;
+  e.box_rows = box_rows;
+  return true;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -236,17 +267,20 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   sa.d = c.d;
   sa.dec_rows = dec_rows;
   sa.dec_bytes_per_key = static_cast<int64_t>(c.h_kv) * c.d * 2 * 2;
-  e = append ? launch_prep(sa, *append, stream) : launch_schedule(sa, stream);
+  // dependent launches hide launch latency; worth it only on short launches
+  const double flops_bound = 4.0 * c.d * c.h_q * static_cast<double>(n_rows) * c.max_kv_len;
+  const bool dependent = flops_bound < kDependentLaunchFlops;
+  e = append ? launch_prep(sa, *append, stream, dependent) : launch_schedule(sa, stream, dependent);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 1;
 
   ExtendTcArgs a;
   std::memset(&a, 0, sizeof a);
-  if (!make_map(&a.tm_q, c.q, c.d, c.h_q, c.total_q, G, tok) ||
-      !make_map(&a.tm_k, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
-      !make_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
-      !make_map(&a.tm_k128, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
-      !make_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN))
+  if (!cached_map(&a.tm_q, c.q, c.d, c.h_q, c.total_q, G, tok) ||
+      !cached_map(&a.tm_k, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
+      !cached_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
+      !cached_map(&a.tm_k128, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
+      !cached_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN))
     return fail(CPE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
   a.page_table = c.page_table; a.qo_indptr = c.qo_indptr; a.prefix_len = c.prefix_len; a.sched = sched;
   a.out = c.out; a.lse = c.lse; a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages;
@@ -259,9 +293,7 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
     a.dec = decode_args(c, L, dec_rows, true, status);
     a.dec_items = dec_rows * c.h_kv * L.max_splits;
   }
-  // dependent launches hide launch latency; worth it only on short launches
-  const double flops_bound = 4.0 * c.d * c.h_q * static_cast<double>(n_rows) * c.max_kv_len;
-  e = launch_extend_tc(a, stream, flops_bound < kDependentLaunchFlops);
+  e = launch_extend_tc(a, stream, dependent);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 2;  // the extend kernel and the merge of key-range parts
   if (dec_rows > 0 && L.max_splits > 1) {

@@ -1,5 +1,7 @@
 // Decode rows (query length 1): the stand-alone split-KV decode kernel (one
 // item of decode_item.cuh per CTA) and the merge of a row's splits.
+#include <atomic>
+
 #include "decode_item.cuh"
 
 namespace cpe {
@@ -40,8 +42,15 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(DecodeArgs a) {
 template <int D>
 cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
   const int smem = DecCfg<D>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<int> ready[64];  // the shared-memory opt-in, once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !ready[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
+  }
   dim3 grid(a.max_splits, a.n_seqs, a.h_kv);
   decode_kernel<D><<<grid, 128, smem, s>>>(a);
   e = cudaGetLastError();

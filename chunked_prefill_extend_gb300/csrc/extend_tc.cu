@@ -51,6 +51,8 @@
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // CPE_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
 // drained, TMEM is freed and the kernel returns.
+#include <atomic>
+
 #include "cpe_device.cuh"
 #include "decode_item.cuh"
 #include "kv_append_row.cuh"
@@ -171,19 +173,31 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars<NK, NV>* bars = reinterpret_cast<Bars<NK, NV>*>(smem + C::kBarOff);
 
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  volatile int* abort = &bars->abort;
+
+  // The tensor-memory allocation touches no global memory: it runs while
+  // the launch before this one (the schedule) finishes.
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
   grid_dependency_wait();    // the schedule (and the round's K/V append) are complete
   grid_launch_dependents();  // the merge kernels may be scheduled as CTAs finish
   const int nc = a.sched.header[1];
   const int n_items = a.sched.header[3];  // item-table entries; CTA c takes c, c + nc, ...
   const int cta = blockIdx.x;
   if (cta >= nc) {  // CTAs past the extend part: decode workers of a fused mixed step, else idle
+    if (warp == 1) tmem_dealloc(tmem, 512);
     if (a.dec_items > 0) decode_worker<D>(a, smem);
     return;
   }
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -207,14 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
 
   if (warp < 4) {
     setmaxnreg_dec_producer();
@@ -764,6 +771,12 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   // pair offsets per sequence (exclusive) and their total; the item table is
   // scratch for them when there are too many sequences for shared memory
   const bool seq_cached = n <= kSchedSeqCache;
+  // Launched as a dependent of the previous kernel, the schedule reads only
+  // the index arrays (which that kernel does not write) until its first
+  // write to the workspace, which the previous launch may still be reading:
+  // the wait comes just before it.  Past the shared-memory caches the
+  // workspace is scratch from the start.
+  if (!seq_cached) grid_dependency_wait();
   int* seq_off = seq_cached ? s_seq_off : a.sched.items;
   int carry = 0;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
@@ -779,29 +792,38 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   const int n_units = min(pairs * a.h_kv, a.capacity);
   if (pairs * a.h_kv > a.capacity && tid == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
   const bool unit_cached = n_units <= kSchedUnitCache;
+  if (seq_cached && !unit_cached) grid_dependency_wait();
   __syncthreads();
   // 1. units (each thread a contiguous range, so unit order is thread order)
   const int per = (n_units + blockDim.x - 1) / blockDim.x;
   const int u_lo = min(n_units, tid * per), u_hi = min(n_units, u_lo + per);
   auto n_kv_of = [&](int u) { return unit_cached ? s_nkv[u] : a.sched.units[u].n_kv; };
-  int W_local = 0, max_local = 0;
-  for (int u = u_lo; u < u_hi; ++u) {
-    const int g = u / pairs;
+  // unit u: sequence, pair and KV head (the sequence by binary search over
+  // the pair offsets)
+  auto unit_of = [&](int u, int& s, int& pair, int& g) {
+    g = u / pairs;
     const int r = u - g * pairs;
     int lo = 0, hi = n;  // the sequence k with seq_off[k] <= r < seq_off[k + 1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) / 2;
       if (seq_off[mid] <= r) lo = mid; else hi = mid;
     }
-    const int s = a.seq_begin + lo;
+    s = a.seq_begin + lo;
     const int np = seq_off[lo + 1] - seq_off[lo];
-    const int pair = np - 1 - (r - seq_off[lo]);
+    pair = np - 1 - (r - seq_off[lo]);
+  };
+  int W_local = 0, max_local = 0;
+  for (int u = u_lo; u < u_hi; ++u) {
+    int s, pair, g;
+    unit_of(u, s, pair, g);
     const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
     const int P = a.prefix_len[s];
     const int i_last = min(E, (2 * pair + 2) * a.tok);  // tokens [0, i_last) of the unit's rows
     const int n_kv = (P + i_last + kBlockN - 1) / kBlockN;
-    a.sched.units[u] = UnitEntry{s, pair, g, n_kv, 1, 0};
-    if (unit_cached) s_nkv[u] = n_kv;
+    if (unit_cached)
+      s_nkv[u] = n_kv;  // the unit entry is written once its parts are known
+    else
+      a.sched.units[u] = UnitEntry{s, pair, g, n_kv, 1, 0};
     W_local += n_kv;
     max_local = max(max_local, n_kv);
   }
@@ -902,10 +924,18 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   }
   int slot_total = 0;
   int slot = block_exclusive_scan(slots_local, &slot_total, warp_sums);
+  if (unit_cached) grid_dependency_wait();  // the workspace writes start here
   for (int u = u_lo; u < u_hi; ++u) {
-    const int pc = unit_parts(n_kv_of(u), T);
-    a.sched.units[u].parts = pc;
-    a.sched.units[u].slot = pc > 1 ? slot : 0;
+    const int n_kv = n_kv_of(u);
+    const int pc = unit_parts(n_kv, T);
+    if (unit_cached) {
+      int s, pair, g;
+      unit_of(u, s, pair, g);
+      a.sched.units[u] = UnitEntry{s, pair, g, n_kv, pc, pc > 1 ? slot : 0};
+    } else {
+      a.sched.units[u].parts = pc;
+      a.sched.units[u].slot = pc > 1 ? slot : 0;
+    }
     slot += pc > 1 ? pc : 0;
   }
   // item counts per (part, size class); this thread's prefix in each run
@@ -985,10 +1015,12 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs
 static_assert(kSchedThreads == kAppendRowsPerBlock * 32, "one warp per appended row");
 __global__ void __launch_bounds__(kSchedThreads) prep_kernel(ScheduleArgs a, KvAppendArgs k) {
   grid_launch_dependents();
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     schedule_body(a);
-  else
+  } else {
+    grid_dependency_wait();  // the previous launch may still read the cache
     append_row(k, (blockIdx.x - 1) * kAppendRowsPerBlock + (threadIdx.x >> 5), threadIdx.x & 31);
+  }
 }
 
 }  // namespace
@@ -997,16 +1029,6 @@ size_t extend_tc_smem_bytes(int d) {
   return d == 128 ? TcCfg<128>::kSmem : TcCfg<64>::kSmem;
 }
 
-cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream_t s) {
-  const int blocks = 1 + (k.total_q + kAppendRowsPerBlock - 1) / kAppendRowsPerBlock;
-  prep_kernel<<<blocks, kSchedThreads, 0, s>>>(a, k);
-  return cudaGetLastError();
-}
 
 // The softmax warpgroups raise their register limit at run time; that only
 // completes if the launch allocated at least kLaunchRegs per thread.
@@ -1037,28 +1059,55 @@ cudaError_t launch_dependent(Kernel kernel, int grid, int block, int smem, cudaS
   return cudaLaunchKernelEx(&cfg, kernel, arg);
 }
 
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, bool dependent) {
+  return launch_dependent(schedule_kernel, 1, kSchedThreads, 0, s, a, dependent);
+}
+
+cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream_t s, bool dependent) {
+  const int blocks = 1 + (k.total_q + kAppendRowsPerBlock - 1) / kAppendRowsPerBlock;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kSchedThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, prep_kernel, a, k);
+}
+
+// Once per device and head size: the register check and the shared-memory
+// opt-in (both hold for the loaded module).
+template <int D>
+cudaError_t prepare_extend() {
+  static std::atomic<int> ready[64];  // 0: not yet, 1: done
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && ready[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = check_regs<D>();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(extend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
+  return cudaSuccess;
+}
+
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
   if (a.n_ctas <= 0) return cudaSuccess;
-  cudaError_t ce = a.d == 128 ? check_regs<128>() : check_regs<64>();
-  if (ce != cudaSuccess) return ce;
+  cudaError_t e = a.d == 128 ? prepare_extend<128>() : prepare_extend<64>();
+  if (e != cudaSuccess) return e;
   if (a.d == 128) {
-    const int smem = TcCfg<128>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, smem, s, a, dependent);
+    e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, TcCfg<128>::kSmem, s, a, dependent);
     if (e != cudaSuccess) return e;
     e = launch_dependent(extend_merge_kernel<128>, a.max_units, 256, 0, s, a, dependent);
-    if (e != cudaSuccess) return e;
   } else {
-    const int smem = TcCfg<64>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, smem, s, a, dependent);
+    e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, TcCfg<64>::kSmem, s, a, dependent);
     if (e != cudaSuccess) return e;
     e = launch_dependent(extend_merge_kernel<64>, a.max_units, 256, 0, s, a, dependent);
-    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace cpe

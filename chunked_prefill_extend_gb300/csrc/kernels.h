@@ -149,13 +149,15 @@ struct KvAppendArgs {
 };
 
 
-cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s);
+// The extend schedule; `dependent` as for launch_extend_tc (the schedule is
+// computed while the previous launch finishes and written after it).
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s, bool dependent);
 // One launch: the extend schedule (block 0) and the round's K/V append (the other blocks).
-cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream_t s);
-// + the merge of split units.  `dependent`: launch both with programmatic
-// stream serialisation (each may be scheduled while the kernel before it
-// finishes), which hides launch latency on short launches; on long ones
-// (measured on cfg5's 1.7 ms launches) it costs about 1 %, so the caller
+cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream_t s, bool dependent);
+// The extend launch + the merge of split units.  `dependent`: launch both with
+// programmatic stream serialisation (each may be scheduled while the kernel
+// before it finishes), which hides launch latency on short launches; on long
+// ones (measured on cfg5's 1.7 ms launches) it costs about 1 %, so the caller
 // turns it on only below kDependentLaunchFlops of extend work.
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent);
 constexpr double kDependentLaunchFlops = 2e11;
