@@ -92,7 +92,11 @@ class Chunked:
         self.idx = {c.index: (torch.tensor([0, c.query_len], dtype=torch.int32, device=device),
                               torch.tensor([c.prefix_len], dtype=torch.int32, device=device)) for c in self.chunks}
         self.out = torch.empty_like(self.req.q)
-        self.ws = cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, device)
+        # two workspaces, alternated between rounds: a round's tile list is
+        # built while the previous round finishes
+        self.wss = [cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, device)
+                    for _ in range(2)]
+        self.ws = self.wss[0]
         self.views = {}
         self.flops = sum(chunk_flops(spec.d, spec.h_q, c.prefix_len, c.query_len) for c in self.chunks)
         self.tokens = sum(c.query_len for c in self.chunks)
@@ -112,7 +116,7 @@ class Chunked:
             views = self.views[key] = tuple(t[a:a + c.query_len] for t in (q, k, v, out))
         qo, pl = self.idx[c.index]
         self.cpe.cpe_mixed_step(views[0], views[1], views[2], self.req.k_cache, self.req.v_cache, self.req.page_table,
-                                qo, pl, 0, c.seq_len, out=views[3], workspace=self.ws)
+                                qo, pl, 0, c.seq_len, out=views[3], workspace=self.wss[c.index & 1])
 
     def step(self, ev=None, q=None, k=None, v=None, out=None):
         cpe, req = self.cpe, self.req
@@ -477,7 +481,7 @@ def run_ours(args, ws, rank, local):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        wl.step(ev=kev)
+        wl.step()  # no events between a step's calls: they would keep its launches from overlapping
         b.record()
         sev.append((a, b))
         if flush is not None:
@@ -532,9 +536,11 @@ def run_ours(args, ws, rank, local):
                                         "frac": wl.decode_bytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                         "ms": dms}}
     else:
-        kms_list = [a.elapsed_time(b) for a, b in zip(*kev)]
-        kms = statistics.mean(kms_list)
-        per_launch = wl.flops / len(wl.chunks)
+        # one round's call, timed over the timed region: its mean duration
+        # there is the step time over the rounds (the calls run back to back)
+        nch = len(wl.chunks)
+        kms = ms_per_step / nch
+        per_launch = wl.flops / nch
         achieved = per_launch / (kms * 1e-3) / 1e12
         pk = peaks["bf16_sustained"]
         traffic = (profiled_traffic(per_launch)
@@ -543,8 +549,14 @@ def run_ours(args, ws, rank, local):
                 "traffic": traffic,
                 "kernel": "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)",
                 "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": per_launch}
-        # per round: the median over the timed steps of that round's call
-        nch = len(wl.chunks)
+        # per round: a pass after the timed region with events around every
+        # call (so each call runs alone); the median over its steps
+        for _ in range(args.steps):
+            wl.step(ev=kev)
+            if flush is not None:
+                flush_l2(flush)
+        torch.cuda.synchronize()
+        kms_list = [a.elapsed_time(b) for a, b in zip(*kev)]
         med = [statistics.median(kms_list[i::nch]) for i in range(nch)]
         curve = [(c.prefix_len, chunk_flops(wl.spec.d, wl.spec.h_q, c.prefix_len, c.query_len) / (t * 1e-3) / 1e12)
                  for c, t in zip(wl.chunks, med)]

@@ -155,6 +155,32 @@ ExtendSched sched_of(const Layout& L, void* ws) {
   return s;
 }
 
+// Whether the previous extend call on stream `s` used workspace `ws` (an
+// unknown stream counts as yes); records `ws` as the stream's latest.  Only
+// then can that call's launches still be reading the schedule this call
+// writes: a call on another workspace lets the schedule be written as soon
+// as it is computed, while the previous call finishes.
+bool reuses_workspace(cudaStream_t s, const void* ws) {
+  struct Entry {
+    cudaStream_t stream;
+    const void* ws;
+  };
+  constexpr int kEntries = 16;
+  static std::mutex mu;
+  static Entry table[kEntries] = {};
+  static int next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (Entry& e : table)
+    if (e.ws != nullptr && e.stream == s) {
+      const bool same = e.ws == ws;
+      e.ws = ws;
+      return same;
+    }
+  table[next] = Entry{s, ws};
+  next = (next + 1) % kEntries;
+  return true;
+}
+
 // SMs of the current device (the persistent extend grid), at most kMaxCtas.
 int persistent_ctas(cudaError_t* err) {
   static int cache[kMaxDevices] = {};
@@ -266,6 +292,7 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   sa.capacity = cap; sa.n_ctas = n_ctas; sa.max_slots = L.slots; sa.sched = sched; sa.status = status;
   sa.d = c.d;
   sa.dec_rows = dec_rows;
+  sa.sched_wait = reuses_workspace(stream, c.workspace) ? 1 : 0;
   sa.dec_bytes_per_key = static_cast<int64_t>(c.h_kv) * c.d * 2 * 2;
   // dependent launches hide launch latency; worth it only on short launches
   const double flops_bound = 4.0 * c.d * c.h_q * static_cast<double>(n_rows) * c.max_kv_len;

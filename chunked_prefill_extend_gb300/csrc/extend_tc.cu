@@ -599,8 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 // unit's rows.  Block b takes unit b; 256 threads, one row each.
 template <int D>
 __global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant__ ExtendTcArgs a) {
-  grid_dependency_wait();  // the extend launch's partials are complete
+  // The next launch may be scheduled now: the next round's schedule does not
+  // depend on this one (its own reads of the cache wait for this launch).
   grid_launch_dependents();
+  grid_dependency_wait();  // the extend launch's partials are complete
   const int n_units = a.sched.header[2];
   const int u = blockIdx.x;
   if (u >= n_units) return;
@@ -772,11 +774,11 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   // scratch for them when there are too many sequences for shared memory
   const bool seq_cached = n <= kSchedSeqCache;
   // Launched as a dependent of the previous kernel, the schedule reads only
-  // the index arrays (which that kernel does not write) until its first
-  // write to the workspace, which the previous launch may still be reading:
-  // the wait comes just before it.  Past the shared-memory caches the
-  // workspace is scratch from the start.
-  if (!seq_cached) grid_dependency_wait();
+  // the index arrays (which that kernel does not write).  When the previous
+  // round used the same workspace (a.sched_wait), that round may still read
+  // it: the wait comes before the first workspace write (at once past the
+  // shared-memory caches, where the workspace is scratch).
+  if (a.sched_wait && !seq_cached) grid_dependency_wait();
   int* seq_off = seq_cached ? s_seq_off : a.sched.items;
   int carry = 0;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
@@ -792,7 +794,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   const int n_units = min(pairs * a.h_kv, a.capacity);
   if (pairs * a.h_kv > a.capacity && tid == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);
   const bool unit_cached = n_units <= kSchedUnitCache;
-  if (seq_cached && !unit_cached) grid_dependency_wait();
+  if (a.sched_wait && seq_cached && !unit_cached) grid_dependency_wait();
   __syncthreads();
   // 1. units (each thread a contiguous range, so unit order is thread order)
   const int per = (n_units + blockDim.x - 1) / blockDim.x;
@@ -924,7 +926,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   }
   int slot_total = 0;
   int slot = block_exclusive_scan(slots_local, &slot_total, warp_sums);
-  if (unit_cached) grid_dependency_wait();  // the workspace writes start here
+  if (a.sched_wait && unit_cached) grid_dependency_wait();  // the workspace writes start here
   for (int u = u_lo; u < u_hi; ++u) {
     const int n_kv = n_kv_of(u);
     const int pc = unit_parts(n_kv, T);
@@ -1007,6 +1009,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
 __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleArgs a) {
   grid_launch_dependents();  // the extend launch may be scheduled (it waits for this one)
   schedule_body(a);
+  grid_dependency_wait();  // this launch completes after the previous one
 }
 
 // A mixed step's prep launch: block 0 builds the extend schedule while the
@@ -1017,6 +1020,7 @@ __global__ void __launch_bounds__(kSchedThreads) prep_kernel(ScheduleArgs a, KvA
   grid_launch_dependents();
   if (blockIdx.x == 0) {
     schedule_body(a);
+    grid_dependency_wait();  // this launch completes after the previous one
   } else {
     grid_dependency_wait();  // the previous launch may still read the cache
     append_row(k, (blockIdx.x - 1) * kAppendRowsPerBlock + (threadIdx.x >> 5), threadIdx.x & 31);

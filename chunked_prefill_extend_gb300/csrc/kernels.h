@@ -94,6 +94,10 @@ struct ScheduleArgs {
   int dec_rows;
   int64_t dec_bytes_per_key;  // K + V bytes one key of one decode row reads
   int d;
+  // 1: the previous call on this stream used the same workspace, so the
+  // schedule is written only once the previous launch has completed; 0: it
+  // is written as soon as it is computed
+  int sched_wait;
 };
 
 struct ExtendTcArgs {

@@ -273,7 +273,12 @@ size_t cpe_workspace_size(int32_t n_seqs, int32_t total_q, int32_t h_q, int32_t 
  * max_kv_len: an upper bound on prefix_len[s] + E_s; sequences above it are
  * not computed and CPE_ERR_DEVICE_ARG is recorded.
  * lse: nullable.  workspace: at least cpe_workspace_size(...) bytes, 256-byte
- * aligned; its contents need not be initialised and are clobbered.
+ * aligned; its contents need not be initialised and are clobbered.  A
+ * workspace serves one stream at a time.  Consecutive calls on one stream
+ * that alternate between two workspaces overlap more: a call's tile list is
+ * built while the previous call finishes.  With one workspace, the tile list
+ * is written only after the previous call is done.  Results are the same
+ * either way.
  * Errors: CPE_ERR_INVALID_ARG / CPE_ERR_UNSUPPORTED / CPE_ERR_CAPACITY before
  * any launch; CPE_ERR_CUDA if a launch fails.
  */

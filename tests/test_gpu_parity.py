@@ -113,20 +113,27 @@ def test_page_permutation_gives_bitwise_equal_output(cpe):
 
 # ---------------------------------------------------------------- chunked == one-shot
 
-def _chunked_run(cpe, spec, device="cuda", one_call=False):
+def _chunked_run(cpe, spec, device="cuda", one_call=False, n_workspaces=0):
     """Every round through cpe_kv_append + cpe_extend_attention, or (one_call)
-    through cpe_mixed_step with no decode rows (append and schedule share a launch)."""
+    through cpe_mixed_step with no decode rows (append and schedule share a launch).
+    n_workspaces: 0 lets each call allocate its own; 1 reuses one workspace for
+    every round; 2 alternates two (the rounds' launches then overlap more)."""
     req = W.make_chunked(spec, device=device)
     chunks, _, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+    wss = [cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, device)
+           for _ in range(n_workspaces)]
     outs = []
     for ch in chunks:
         q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
         qo, pl = i32([0, ch.query_len]), i32([ch.prefix_len])
+        ws = wss[ch.index % len(wss)] if wss else None
         if one_call:
-            out, _ = cpe.cpe_mixed_step(q, k, v, req.k_cache, req.v_cache, req.page_table, qo, pl, 0, ch.seq_len)
+            out, _ = cpe.cpe_mixed_step(q, k, v, req.k_cache, req.v_cache, req.page_table, qo, pl, 0, ch.seq_len,
+                                        workspace=ws)
         else:
             cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, qo, pl)
-            out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, qo, pl, ch.seq_len)
+            out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, qo, pl, ch.seq_len,
+                                              workspace=ws)
         outs.append(out)
     _status_ok(cpe)
     return req, chunks, torch.cat(outs)
@@ -222,12 +229,19 @@ def test_many_short_sequences(cpe):
 # ---------------------------------------------------------------- full-size workloads
 
 def test_cfg2_full(cpe):
-    """Every row of cfg2, each round in one call as the benchmark runs it."""
+    """Every row of cfg2, each round in one call as the benchmark runs it (two
+    workspaces alternated, so a round's tile list is written while the previous
+    round runs); one shared workspace gives the same bits."""
     spec = W.CONFIGS["cfg2"]
-    req, chunks, out = _chunked_run(cpe, spec, one_call=True)
+    req, chunks, out = _chunked_run(cpe, spec, one_call=True, n_workspaces=2)
     assert [c.query_len for c in chunks] == [512] * 7 + [416]
     one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
     check_close(out, one, "cfg2 all rows")
+    _, _, out1 = _chunked_run(cpe, spec, one_call=True, n_workspaces=1)
+    assert torch.equal(out, out1)
+    # the separate append + extend calls, alternating too
+    _, _, out2 = _chunked_run(cpe, spec, n_workspaces=2)
+    assert torch.equal(out, out2)
 
 
 def _sampled_rounds(cpe, spec, round_ids, n_rows, seed):
