@@ -749,11 +749,14 @@ __device__ void block_scan_n(int (&v)[N], int (*scratch)[N], int* totals) {
 // 1. Units: per KV head, each sequence's units last-first (the longest key
 //    range first), two query tiles each.
 // 2. Parts: candidate target lengths T = ceil(longest unit / S), S = 1..8; a
-//    unit of n_kv key tiles is cut into ceil(n_kv / T) parts.  The candidate
-//    whose parts fill whole waves of CTAs best (work / (CTAs x T x waves)) is
-//    taken; a larger S must win clearly (3 %), fit the partial slots and keep
-//    parts of kMinTilesPerPart tiles on average.  Units of equal length thus
-//    get the same number of parts; unequal ones get parts of similar length.
+//    unit of n_kv key tiles is cut into ceil(n_kv / T) parts.  Each candidate
+//    is costed as its waves of CTAs times (T + the fixed cost of an item), plus
+//    the merge when units are cut, in key-tile times; the cheapest is taken (a
+//    larger S must win clearly, by 3 %, and fit the partial slots).  On a
+//    launch of one wave that is the longest item, which cutting shortens while
+//    idle SMs take the parts; on long launches it is how well the parts fill
+//    whole waves.  Units of equal length get the same number of parts;
+//    unequal ones get parts of similar length.
 // 3. Order: parts in kSizeBuckets size classes, largest first; within a class
 //    part-major, then unit order (so CTAs running at the same time stream the
 //    same key range of a KV head).  Position k of that order goes to CTA
@@ -901,17 +904,17 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   const int* sums16 = totals;
   if (tid == 0) {
     int best_T = max(1, n_max);
-    float best_eff = -1.f;
+    float best_t = 3.4e38f;
     for (int S = 1; S <= kMaxParts; ++S) {
       const int T = max(1, (n_max + S - 1) / S);
       const int items = sums16[S - 1];
-      if (S > 1 && (sums16[kMaxParts + S - 1] > a.max_slots || W < items * kMinTilesPerPart)) break;
+      if (S > 1 && sums16[kMaxParts + S - 1] > a.max_slots) break;
       const int ncp = max(1, min(n_ext, items));
       const int waves = (items + ncp - 1) / ncp;
-      const float eff = static_cast<float>(W) / (static_cast<float>(ncp) * T * waves);
-      if (eff > best_eff + 0.03f) {  // more parts only when they fill the waves clearly better
+      const float t = waves * (T + kItemCostTiles) + (S > 1 ? kMergeCostTiles : 0.f);
+      if (t < best_t * 0.97f) {  // more parts only when they are clearly faster
         best_T = T;
-        best_eff = eff;
+        best_t = t;
       }
     }
     s_T = best_T;

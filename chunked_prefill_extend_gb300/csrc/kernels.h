@@ -15,7 +15,13 @@ constexpr int kDecodeSplit = 2048;  // keys per decode split
 
 constexpr int kMaxCtas = 160;        // upper bound of the persistent extend grid (SMs used)
 constexpr int kMaxParts = 8;         // key-range parts a unit may be cut into
-constexpr int kMinTilesPerPart = 4;  // parts shorter than this (on average) are not used
+// Costs the extend schedule weighs against key-tile times, measured on GB300
+// at d = 128 from rounds of 512 queries: an item's fixed cost (its query
+// tiles' load, the pipeline's fill and drain, the output's store), and the
+// merge of units cut into parts (the partial results' writes and the merge
+// launch after the extend launch has drained).
+constexpr float kItemCostTiles = 3.0f;
+constexpr float kMergeCostTiles = 6.0f;
 constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first order
 constexpr int kItemPartShift = 24;   // item = unit | part << kItemPartShift
 constexpr int kMaxSlots = 1024;      // partial-result slots in the workspace
