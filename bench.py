@@ -135,41 +135,70 @@ class Chunked:
                 ev[1][-1].record()
         return out
 
-    def host_io(self):
-        return [self.req.q, self.req.k, self.req.v], self.out
+    def e2e_setup(self, device):
+        """Host side of the end-to-end step: each round's q, k and v rows packed
+        in one pinned buffer (one upload per round), two device sets that
+        consecutive steps alternate (a step's uploads overlap the previous
+        step's work), and a pinned output.  Returns the bytes moved per step."""
+        req = self.req
+        self.e2e = []
+        for c in self.chunks:
+            a = c.prefix_len - self.cached
+            rows = [t[a:a + c.query_len] for t in (req.q, req.k, req.v)]
+            sizes = [r.numel() * r.element_size() for r in rows]
 
-    def step_e2e(self, host_in, dev_in, host_out, dev_out, h2d, d2h):
+            def views(buf, rows=rows, sizes=sizes):
+                out, off = [], 0
+                for r, n in zip(rows, sizes):  # every offset is a multiple of 256 bytes
+                    out.append(buf[off:off + n].view(r.dtype).view(r.shape))
+                    off += n
+                return out
+            host = torch.empty(sum(sizes), dtype=torch.uint8, pin_memory=True)
+            for hv, r in zip(views(host), rows):
+                hv.copy_(r.cpu())
+            devs = [torch.empty(sum(sizes), dtype=torch.uint8, device=device) for _ in range(2)]
+            self.e2e.append((c, host, devs, [views(d) for d in devs], a))
+        self.e2e_out = [torch.empty_like(self.out) for _ in range(2)]
+        self.e2e_host_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        self.e2e_out_views = [[(o[a:a + c.query_len], self.e2e_host_out[a:a + c.query_len])
+                               for c, _, _, _, a in self.e2e] for o in self.e2e_out]
+        return sum(h.numel() for _, h, _, _, _ in self.e2e), self.e2e_host_out.numel() * self.e2e_host_out.element_size()
+
+    def step_e2e(self, s, h2d, d2h, free_ev):
         """One step from pinned host inputs to pinned host output through the
-        public calls: chunk t's rows go host->device on one stream and chunk
-        t-1's output device->host on another while chunk t computes."""
+        public calls, on device set s: round t's rows go host->device on one
+        stream and its output device->host on another, while other rounds
+        compute.  free_ev: when set s's previous step is done with it.  Returns
+        the event after this step's last download."""
         cpe, req = self.cpe, self.req
         main = torch.cuda.current_stream()
-        chunks, _, _ = cpe.cpe_plan_chunks(self.spec.input_len, self.spec.hit_rate, self.spec.chunk)
-        chunks = chunks[self.rounds[0]:self.rounds[1]]
-        h2d.wait_stream(main)  # the previous step is done with the device buffers
+        cpe.cpe_plan_chunks(self.spec.input_len, self.spec.hit_rate, self.spec.chunk)
+        if free_ev is not None:
+            h2d.wait_event(free_ev)
         ev_in = []
         with torch.cuda.stream(h2d):
-            for c in chunks:
-                a = c.prefix_len - self.cached
-                for d, h in zip(dev_in, host_in):
-                    d[a:a + c.query_len].copy_(h[a:a + c.query_len], non_blocking=True)
+            for _, host, devs, _, _ in self.e2e:
+                devs[s].copy_(host, non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(h2d)
                 ev_in.append(e)
         ev_out = []
-        q, k, v = dev_in
-        for c, e in zip(chunks, ev_in):
+        for (c, _, _, views, _), (o, _), e in zip(self.e2e, self.e2e_out_views[s], ev_in):
             main.wait_event(e)
-            self.chunk_call(c, q, k, v, dev_out)
+            qo, pl = self.idx[c.index]
+            q, k, v = views[s]
+            cpe.cpe_mixed_step(q, k, v, req.k_cache, req.v_cache, req.page_table, qo, pl, 0, c.seq_len, out=o,
+                               workspace=self.wss[c.index & 1])
             e2 = torch.cuda.Event()
             e2.record(main)
             ev_out.append(e2)
         with torch.cuda.stream(d2h):
-            for c, e in zip(chunks, ev_out):
+            for (o, ho), e in zip(self.e2e_out_views[s], ev_out):
                 d2h.wait_event(e)
-                a = c.prefix_len - self.cached
-                host_out[a:a + c.query_len].copy_(dev_out[a:a + c.query_len], non_blocking=True)
-        main.wait_stream(d2h)
+                ho.copy_(o, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(d2h)
+        return done
 
     def kernel_units(self):
         return self.flops / len(self.chunks), "flop"
@@ -592,41 +621,53 @@ def run_ours(args, ws, rank, local):
 def e2e_measure(wl, args, device, ws):
     """The same metric through the public API with pinned host inputs copied in
     and the output copied back inside the timed region (every step)."""
-    ins, out_dev = wl.host_io()
-    host_in = [t.cpu().pin_memory() for t in ins]
-    host_out = torch.empty(out_dev.shape, dtype=out_dev.dtype, pin_memory=True)
-    dev_in = [torch.empty_like(t) for t in ins]
-    dev_out = torch.empty_like(out_dev)
     h2d = torch.cuda.Stream(device=device)
     d2h = torch.cuda.Stream(device=device)
+    if hasattr(wl, "e2e_setup"):
+        bytes_in, bytes_out = wl.e2e_setup(device)
+        done = [None, None]
+        count = [0]
 
-    def one_step():
-        if hasattr(wl, "step_e2e"):
-            wl.step_e2e(host_in, dev_in, host_out, dev_out, h2d, d2h)
-        else:
+        def one_step():
+            s = count[0] & 1
+            done[s] = wl.step_e2e(s, h2d, d2h, done[s])
+            count[0] += 1
+        copies = ("pinned host buffers, each round's q/k/v rows in one; per-round uploads and downloads on two "
+                  "side streams overlapping compute, consecutive steps on alternate device buffers")
+    else:
+        ins, out_dev = wl.host_io()
+        host_in = [t.cpu().pin_memory() for t in ins]
+        host_out = torch.empty(out_dev.shape, dtype=out_dev.dtype, pin_memory=True)
+        dev_in = [torch.empty_like(t) for t in ins]
+        dev_out = torch.empty_like(out_dev)
+        bytes_in = sum(t.numel() * t.element_size() for t in host_in)
+        bytes_out = host_out.numel() * host_out.element_size()
+
+        def one_step():
             for d, h in zip(dev_in, host_in):
                 d.copy_(h, non_blocking=True)
             wl.step(q=dev_in[0], k=dev_in[1], v=dev_in[2], out=dev_out)
             host_out.copy_(dev_out, non_blocking=True)
+        copies = "pinned host buffers; H2D, step, D2H in order"
 
     n = max(3, min(args.steps, 10))
     for _ in range(2):
         one_step()
+    torch.cuda.current_stream().wait_stream(d2h)
     torch.cuda.synchronize()
     barrier(ws)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record()
+    h2d.wait_stream(torch.cuda.current_stream())  # the first upload starts inside the timed region
     for _ in range(n):
         one_step()
+    torch.cuda.current_stream().wait_stream(d2h)  # every step's download is inside the timed region
     b.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b) / n, ws, device)
     return {"value": wl.flops * ws / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
-            "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": ms,
-            "copies": "pinned host buffers; per-chunk H2D and D2H on two side streams overlapping compute"
-            if hasattr(wl, "step_e2e") else "pinned host buffers; H2D, step, D2H in order"}
+            "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out, "ms_per_step": ms, "copies": copies}
 
 
 def cpu_baseline(wl, args):
