@@ -440,9 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (!mbar_wait(&bars->s_full[t], sc & 1, abort, a.wait_ns, a.status, kDetailSFull)) { ok = false; break; }
         ++sc;
         tc_fence_after();
-        // the whole S row: four loads in flight, one wait
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        {
+        const int kb = j * kBlockN;
+        float sv[kBlockN];
+        // the whole S row: four loads in flight, one wait; masked where the
+        // tile crosses the diagonal or the end
+        auto load_s = [&]() {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
           const uint32_t sa = tmem + lane_base + s_col;
           tmem_ld32(sa, r0);
           tmem_ld32(sa + 32, r1);
@@ -452,61 +455,79 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           reg_dep(r1);
           reg_dep(r2);
           reg_dep(r3);
-        }
-        float sv[kBlockN];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          sv[x] = __uint_as_float(r0[x]);
-          sv[32 + x] = __uint_as_float(r1[x]);
-          sv[64 + x] = __uint_as_float(r2[x]);
-          sv[96 + x] = __uint_as_float(r3[x]);
-        }
-        const int kb = j * kBlockN;
-        if (kb + kBlockN - 1 > it.P + i0t) {  // tile crosses the diagonal or the end: mask
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c)
-            if (kb + c > lim) sv[c] = -INFINITY;
-        }
-        // row max: 16 independent chains of 3-input maxes, then a tree
-        float mx[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          mx[q] = fmax3(sv[q], sv[q + 16], sv[q + 32]);
-          mx[q] = fmax3(mx[q], sv[q + 48], sv[q + 64]);
-          mx[q] = fmax3(mx[q], sv[q + 80], sv[q + 96]);
-          mx[q] = fmaxf(mx[q], sv[q + 112]);
-        }
-#pragma unroll
-        for (int q = 0; q < 5; ++q) mx[q] = fmax3(mx[q], mx[q + 5], mx[q + 10]);
-        const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmaxf(mx[3], mx[4]), mx[15]) * sl2;
-        const bool grow = m_tile > m_run + 8.0f;
-        const float m_new = grow ? m_tile : m_run;
-        const float factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
-        m_run = m_new;
-        const float mbase = (m_run == -INFINITY) ? 0.f : m_run;
-        // p = 2^(s * scale * log2 e - m): scale-and-subtract and the row sum on pairs
-        const float2 sl2x2 = make_float2(sl2, sl2);
-        const float2 negm = make_float2(-mbase, -mbase);
-        float2 acc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < kBlockN / 64; ++c) {
-          uint32_t pk[32];
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
-            const float2 z = __ffma2_rn(make_float2(sv[c * 64 + 2 * x], sv[c * 64 + 2 * x + 1]), sl2x2, negm);
+            sv[x] = __uint_as_float(r0[x]);
+            sv[32 + x] = __uint_as_float(r1[x]);
+            sv[64 + x] = __uint_as_float(r2[x]);
+            sv[96 + x] = __uint_as_float(r3[x]);
+          }
+          if (kb + kBlockN - 1 > it.P + i0t) {
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c)
+              if (kb + c > lim) sv[c] = -INFINITY;
+          }
+        };
+        load_s();
+        // p = 2^(s * scale * log2 e - m): scale-and-subtract and the row sum
+        // on pairs; P packed to bf16 pairs in pk0 (columns 0-63) and pk1
+        uint32_t pk0[32], pk1[32];
+        float sum = 0.f;
+        auto exps = [&](float mbase) {
+          const float2 sl2x2 = make_float2(sl2, sl2);
+          const float2 negm = make_float2(-mbase, -mbase);
+          float2 acc[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int x = 0; x < kBlockN / 2; ++x) {
+            const float2 z = __ffma2_rn(make_float2(sv[2 * x], sv[2 * x + 1]), sl2x2, negm);
             const float2 pp = make_float2(fast_exp2(z.x), fast_exp2(z.y));
             acc[x & 3] = __fadd2_rn(acc[x & 3], pp);
-            pk[x] = pack_bf16x2(pp.x, pp.y);
+            (x < 32 ? pk0 : pk1)[x & 31] = pack_bf16x2(pp.x, pp.y);
           }
-          tmem_st32(tmem + lane_base + s_col + c * 32, pk);
+          const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+          const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+          const float2 a03 = __fadd2_rn(a01, a23);
+          sum = a03.x + a03.y;
+        };
+        // Past the item's first tile the exponentials are taken against the
+        // running max at once: the tile's own max matters only if a weight
+        // would pass 2^16, which the row sum shows (a sum of at most 2^16
+        // bounds every weight; a non-finite one, from a row with no key yet,
+        // fails too).  Otherwise (and on the first tile) the max is reduced
+        // and the running max raised when the tile's exceeds it by more than
+        // 8 (log2 units), with O and l rescaled: the lazy rescale.
+        float factor = 1.0f;
+        bool grow = false;
+        bool done = false;
+        if (j > it.kv_lo) {
+          exps(m_run);
+          done = __all_sync(0xffffffffu, sum <= 65536.0f);
+          if (!done) load_s();  // the registers were spent; S is still in TMEM
         }
-        const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-        const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-        const float2 a03 = __fadd2_rn(a01, a23);
-        const float sum = a03.x + a03.y;
+        if (!done) {
+          // row max: 16 independent chains of 3-input maxes, then a tree
+          float mx[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            mx[q] = fmax3(sv[q], sv[q + 16], sv[q + 32]);
+            mx[q] = fmax3(mx[q], sv[q + 48], sv[q + 64]);
+            mx[q] = fmax3(mx[q], sv[q + 80], sv[q + 96]);
+            mx[q] = fmaxf(mx[q], sv[q + 112]);
+          }
+#pragma unroll
+          for (int q = 0; q < 5; ++q) mx[q] = fmax3(mx[q], mx[q + 5], mx[q + 10]);
+          const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmaxf(mx[3], mx[4]), mx[15]) * sl2;
+          grow = m_tile > m_run + 8.0f;
+          const float m_new = grow ? m_tile : m_run;
+          factor = grow ? fast_exp2(m_run - m_new) : 1.0f;
+          m_run = m_new;
+          exps((m_run == -INFINITY) ? 0.f : m_run);
+        }
         l_run = l_run * factor + sum;
+        tmem_st32(tmem + lane_base + s_col, pk0);
+        tmem_st32(tmem + lane_base + s_col + 32, pk1);
         // The S barrier fired after every earlier MMA, so O_t holds the previous
         // PV: rescale it here, before the next PV is issued.
         if (j > it.kv_lo && __any_sync(0xffffffffu, grow)) {
