@@ -3,6 +3,7 @@
 // the contract of every entry point.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -117,7 +118,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t header_off, units_off, items_off, partial_off, part_o_off, part_ml_off, total;
+  size_t header_off, units_off, items_off, split_off, partial_off, part_o_off, part_ml_off, total;
   int unit_capacity, max_splits, slots;
 };
 
@@ -136,8 +137,9 @@ Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int m
   L.header_off = 0;
   L.units_off = 256;
   L.items_off = L.units_off + align256(static_cast<size_t>(cap) * sizeof(UnitEntry));
-  L.partial_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(int));
   L.slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
+  L.split_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(int));
+  L.partial_off = L.split_off + align256(static_cast<size_t>(L.slots / 2 + 1) * sizeof(UnitEntry));
   const size_t parts = static_cast<size_t>(n_seqs) * h_q * L.max_splits;
   L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_bytes(d));
   L.part_ml_off = L.part_o_off + align256(parts * d * sizeof(float));
@@ -151,6 +153,7 @@ ExtendSched sched_of(const Layout& L, void* ws) {
   s.header = reinterpret_cast<int*>(b + L.header_off);
   s.units = reinterpret_cast<UnitEntry*>(b + L.units_off);
   s.items = reinterpret_cast<int*>(b + L.items_off);
+  s.split = reinterpret_cast<UnitEntry*>(b + L.split_off);
   s.partial = b + L.partial_off;
   return s;
 }
@@ -315,7 +318,7 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   a.scale_log2 = c.sm_scale * 1.4426950408889634f;
   a.wait_ns = static_cast<uint64_t>(g_wait_ns.load() < 0 ? 0 : g_wait_ns.load());
   a.n_ctas = n_ctas;
-  a.max_units = cap;
+  a.max_split = std::max(1, std::min(cap, L.slots / 2));  // cut units: at most one per unit, two slots each
   if (dec_rows > 0) {
     a.dec = decode_args(c, L, dec_rows, true, status);
     a.dec_items = dec_rows * c.h_kv * L.max_splits;

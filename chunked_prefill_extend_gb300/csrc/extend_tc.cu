@@ -51,6 +51,7 @@
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // CPE_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
 // drained, TMEM is freed and the kernel returns.
+#include <algorithm>
 #include <atomic>
 
 #include "cpe_device.cuh"
@@ -616,70 +617,107 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   }
 }
 
-// Combine the parts of each unit (the online-softmax LSE rule) and write the
-// unit's rows.  Block b takes unit b; 256 threads, one row each.
+// Work item w of extend_merge_kernel (see there).
 template <int D>
-__global__ void __launch_bounds__(256) extend_merge_kernel(const __grid_constant__ ExtendTcArgs a) {
+__device__ __forceinline__ void merge_rows(const ExtendTcArgs& a, int w) {
+  const UnitEntry e = a.sched.split[w / kMergeRowGroups];
+  const int len = (e.n_kv + e.parts - 1) / e.parts;
+  const int live = (e.n_kv + len - 1) / len;  // parts that hold key tiles
+  const int q0 = a.qo_indptr[e.seq];
+  const int E = a.qo_indptr[e.seq + 1] - q0;
+  constexpr int kW = D / 64;  // 32-bit words (bf16 pairs) per lane and row
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int row0 = (w % kMergeRowGroups) * 32 + warp * 4;
+  const uint8_t* slot0 = a.sched.partial + static_cast<size_t>(e.slot) * partial_slot_bytes(D);
+#pragma unroll 1
+  for (int rr = 0; rr < 4; rr += 2) {
+    float m[2][kMaxParts], l[2][kMaxParts];
+    uint32_t v[2][kMaxParts][kW];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int R = row0 + rr + h;
+#pragma unroll
+      for (int p = 0; p < kMaxParts; ++p) {
+        if (p < live) {
+          const uint8_t* slot = slot0 + static_cast<size_t>(p) * partial_slot_bytes(D);
+          const float* ml = reinterpret_cast<const float*>(slot + static_cast<size_t>(kUnitRows) * D * 2);
+          m[h][p] = ml[R];
+          l[h][p] = ml[kUnitRows + R];
+          const uint32_t* row = reinterpret_cast<const uint32_t*>(slot + static_cast<size_t>(R) * D * 2) + lane * kW;
+          if constexpr (kW == 2) {
+            const uint2 x = *reinterpret_cast<const uint2*>(row);
+            v[h][p][0] = x.x;
+            v[h][p][kW - 1] = x.y;
+          } else {
+            v[h][p][0] = row[0];
+          }
+        } else {
+          m[h][p] = -INFINITY;
+          l[h][p] = 0.f;
+#pragma unroll
+          for (int w = 0; w < kW; ++w) v[h][p][w] = 0u;
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int R = row0 + rr + h;
+      const int t = R / kBlockM;
+      const int r = R % kBlockM;
+      const int i = (2 * e.pair + t) * a.tok + r / a.group;
+      if (i >= E) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int p = 0; p < kMaxParts; ++p)
+        if (l[h][p] > 0.f) M = fmaxf(M, m[h][p]);
+      float wsum = 0.f;
+      float o[2 * kW];
+#pragma unroll
+      for (int c = 0; c < 2 * kW; ++c) o[c] = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMaxParts; ++p) {
+        if (!(l[h][p] > 0.f)) continue;  // this part holds no key of this row
+        const float wgt = fast_exp2(m[h][p] - M) * l[h][p];
+        wsum += wgt;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {  // bf16 -> fp32 is a shift
+          o[2 * w] += wgt * __uint_as_float(v[h][p][w] << 16);
+          o[2 * w + 1] += wgt * __uint_as_float(v[h][p][w] & 0xffff0000u);
+        }
+      }
+      const float inv = 1.f / wsum;
+      const int head = e.kv_head * a.group + r % a.group;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                  (static_cast<int64_t>(q0 + i) * a.h_q + head) * D) + lane * kW;
+      if constexpr (kW == 2) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
+      } else {
+        dst[0] = pack_bf16x2(o[0] * inv, o[1] * inv);
+      }
+      if (lane == 0 && a.lse != nullptr)
+        a.lse[static_cast<int64_t>(q0 + i) * a.h_q + head] = (M + __log2f(wsum)) * 0.69314718055994531f;
+    }
+  }
+}
+
+// Combine the parts of each cut unit (the online-softmax LSE rule: weights
+// 2^(m_p - M) * l_p of the normalised part outputs) and write its rows.  The
+// grid is persistent (two blocks per SM, all resident, so the next launch is
+// released at once); block b takes work items b, b + gridDim.x, ..., item
+// w being rows [32 g, 32 g + 32), g = w mod kMergeRowGroups, of the
+// (w / kMergeRowGroups)-th cut unit.  Each of the 8 warps takes four of the
+// rows, two at a time, with every part's loads in flight at once; lane l holds
+// columns [l D / 32, (l + 1) D / 32), so one part of one row is one coalesced
+// read.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) extend_merge_kernel(const __grid_constant__ ExtendTcArgs a) {
   // The next launch may be scheduled now: the next round's schedule does not
   // depend on this one (its own reads of the cache wait for this launch).
   grid_launch_dependents();
   grid_dependency_wait();  // the extend launch's partials are complete
-  const int n_units = a.sched.header[2];
-  const int u = blockIdx.x;
-  if (u >= n_units) return;
-  const UnitEntry e = a.sched.units[u];
-  const int parts = e.parts;
-  if (parts <= 1) return;
-  const int len = (e.n_kv + parts - 1) / parts;
-  const int R = threadIdx.x;
-  const int t = R / kBlockM;
-  const int r = R % kBlockM;
-  const int q0 = a.qo_indptr[e.seq];
-  const int E = a.qo_indptr[e.seq + 1] - q0;
-  const int i = (2 * e.pair + t) * a.tok + r / a.group;
-  if (i >= E) return;
-  auto slot_of = [&](int p) { return a.sched.partial + static_cast<size_t>(e.slot + p) * partial_slot_bytes(D); };
-  auto ml_of = [&](int p) { return reinterpret_cast<const float*>(slot_of(p) + static_cast<size_t>(kUnitRows) * D * 2); };
-  float M = -INFINITY;
-  for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
-    const float* ml = ml_of(p);
-    if (ml[kUnitRows + R] > 0.f) M = fmaxf(M, ml[R]);
-  }
-  float wsum = 0.f;
-  float o[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) o[d] = 0.f;
-  for (int p = 0; p < parts && p * len < e.n_kv; ++p) {
-    const float* ml = ml_of(p);
-    const float l = ml[kUnitRows + R];
-    if (!(l > 0.f)) continue;  // this part holds no key of this row
-    const float w = fast_exp2(ml[R] - M) * l;
-    wsum += w;
-    const uint4* row = reinterpret_cast<const uint4*>(slot_of(p) + static_cast<size_t>(R) * D * 2);
-#pragma unroll
-    for (int d8 = 0; d8 < D / 8; ++d8) {  // eight bf16 per vector; bf16 -> fp32 is a shift
-      const uint4 v = row[d8];
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        o[8 * d8 + 2 * k] += w * __uint_as_float(u[k] << 16);
-        o[8 * d8 + 2 * k + 1] += w * __uint_as_float(u[k] & 0xffff0000u);
-      }
-    }
-  }
-  const float inv = 1.f / wsum;
-  const int head = e.kv_head * a.group + r % a.group;
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(q0 + i) * a.h_q + head) * D);
-#pragma unroll
-  for (int x = 0; x < D / 8; ++x) {
-    uint4 v;
-    v.x = pack_bf16x2(o[8 * x + 0] * inv, o[8 * x + 1] * inv);
-    v.y = pack_bf16x2(o[8 * x + 2] * inv, o[8 * x + 3] * inv);
-    v.z = pack_bf16x2(o[8 * x + 4] * inv, o[8 * x + 5] * inv);
-    v.w = pack_bf16x2(o[8 * x + 6] * inv, o[8 * x + 7] * inv);
-    dst[x] = v;
-  }
-  if (a.lse != nullptr) a.lse[static_cast<int64_t>(q0 + i) * a.h_q + head] = (M + __log2f(wsum)) * 0.69314718055994531f;
+  const int n_work = a.sched.header[7] * kMergeRowGroups;
+  for (int w = blockIdx.x; w < n_work; w += gridDim.x) merge_rows<D>(a, w);
 }
 
 // Block-wide exclusive prefix sum (blockDim.x a multiple of 32, <= 1024).
@@ -943,25 +981,32 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   __syncthreads();
   const int T = s_T;
   // 3. parts and partial slots per unit (slots in unit order, split units only)
-  int slots_local = 0;
+  // (and the cut units' ranks in the list the merge kernel walks)
+  int sc2[2] = {0, 0};
   for (int u = u_lo; u < u_hi; ++u) {
     const int pc = unit_parts(n_kv_of(u), T);
-    slots_local += pc > 1 ? pc : 0;
+    sc2[0] += pc > 1 ? pc : 0;
+    sc2[1] += pc > 1 ? 1 : 0;
   }
-  int slot_total = 0;
-  int slot = block_exclusive_scan(slots_local, &slot_total, warp_sums);
+  block_scan_n<2>(sc2, reinterpret_cast<int (*)[2]>(&scratch[0][0]), totals);
+  int slot = sc2[0], split_rank = sc2[1];
+  const int n_split = totals[1];
   if (a.sched_wait && unit_cached) grid_dependency_wait();  // the workspace writes start here
   for (int u = u_lo; u < u_hi; ++u) {
     const int n_kv = n_kv_of(u);
     const int pc = unit_parts(n_kv, T);
+    UnitEntry e;
     if (unit_cached) {
       int s, pair, g;
       unit_of(u, s, pair, g);
-      a.sched.units[u] = UnitEntry{s, pair, g, n_kv, pc, pc > 1 ? slot : 0};
+      e = UnitEntry{s, pair, g, n_kv, pc, pc > 1 ? slot : 0};
     } else {
-      a.sched.units[u].parts = pc;
-      a.sched.units[u].slot = pc > 1 ? slot : 0;
+      e = a.sched.units[u];
+      e.parts = pc;
+      e.slot = pc > 1 ? slot : 0;
     }
+    a.sched.units[u] = e;
+    if (pc > 1) a.sched.split[split_rank++] = e;
     slot += pc > 1 ? pc : 0;
   }
   // item counts per (part, size class); this thread's prefix in each run
@@ -1027,6 +1072,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
     a.sched.header[4] = T;
     a.sched.header[5] = n_items;
     a.sched.header[6] = 0;
+    a.sched.header[7] = n_split;
   }
 }
 
@@ -1126,14 +1172,16 @@ cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool depende
   if (a.n_ctas <= 0) return cudaSuccess;
   cudaError_t e = a.d == 128 ? prepare_extend<128>() : prepare_extend<64>();
   if (e != cudaSuccess) return e;
+  // the merge's persistent grid: two blocks per SM, fewer if there cannot be that much work
+  const int merge_grid = std::max(1, std::min(a.max_split * kMergeRowGroups, 2 * a.n_ctas));
   if (a.d == 128) {
     e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, TcCfg<128>::kSmem, s, a, dependent);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(extend_merge_kernel<128>, a.max_units, 256, 0, s, a, dependent);
+    e = launch_dependent(extend_merge_kernel<128>, merge_grid, kMergeThreads, 0, s, a, dependent);
   } else {
     e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, TcCfg<64>::kSmem, s, a, dependent);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(extend_merge_kernel<64>, a.max_units, 256, 0, s, a, dependent);
+    e = launch_dependent(extend_merge_kernel<64>, merge_grid, kMergeThreads, 0, s, a, dependent);
   }
   return e;
 }

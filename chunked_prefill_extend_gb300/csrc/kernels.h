@@ -26,6 +26,8 @@ constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first o
 constexpr int kItemPartShift = 24;   // item = unit | part << kItemPartShift
 constexpr int kMaxSlots = 1024;      // partial-result slots in the workspace
 constexpr int kUnitRows = 2 * kBlockM;
+constexpr int kMergeRowGroups = 8;  // merge work items per cut unit (32 rows each)
+constexpr int kMergeThreads = 256;  // merge block: 8 warps, four rows each
 
 struct UnitEntry {  // one extend work unit: two query tiles of one sequence and KV head
   int seq;
@@ -44,11 +46,12 @@ struct UnitEntry {  // one extend work unit: two query tiles of one sequence and
 struct ExtendSched {
   int* header;          // [0] total key tiles, [1] CTAs used, [2] units, [3] item table length
                         // (a multiple of [1]), [4] target part length, [5] items, [6] next
-                        // decode item of a fused mixed step
+                        // decode item of a fused mixed step, [7] units cut into parts
   UnitEntry* units;     // [capacity]
   int* items;           // [item capacity]
   uint8_t* partial;     // slots of partial_slot_bytes(d): O [256 x d] bf16 (normalised), then m [256]
                         // (log2) and l [256] fp32
+  UnitEntry* split;     // the units cut into parts, in unit order (header[7] of them)
 };
 
 __host__ __device__ constexpr size_t partial_slot_bytes(int d) {
@@ -122,7 +125,7 @@ struct ExtendTcArgs {
   float scale_log2;
   uint64_t wait_ns;
   int n_ctas;
-  int max_units;  // unit capacity (the merge kernel's grid)
+  int max_split;  // units that may be cut into parts (the merge kernel's grid / kMergeRowGroups)
   // fused mixed step: CTAs past the extend part run these decode items
   // ((sequence x KV head) x split, split fastest), taken from header[6]
   DecodeArgs dec;
