@@ -829,7 +829,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   __shared__ int run_start[kRuns];
   __shared__ int s_seq_off[kSchedSeqCache + 1];
   __shared__ int s_nkv[kSchedUnitCache];
-  __shared__ int s_T, s_items;
+  __shared__ int s_T, s_items, s_fill;
   const int tid = threadIdx.x;
   const int n = a.seq_end - a.seq_begin;
   // pair offsets per sequence (exclusive) and their total; the item table is
@@ -962,39 +962,75 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   block_scan_n<2 * kMaxParts>(v16, reinterpret_cast<int (*)[2 * kMaxParts]>(&scratch[0][0]), totals);
   const int* sums16 = totals;
   if (tid == 0) {
-    int best_T = max(1, n_max);
+    int best_T = max(1, n_max), best_fill = 0;
     float best_t = 3.4e38f;
     for (int S = 1; S <= kMaxParts; ++S) {
       const int T = max(1, (n_max + S - 1) / S);
       const int items = sums16[S - 1];
-      if (S > 1 && sums16[kMaxParts + S - 1] > a.max_slots) break;
+      const int slots = S > 1 ? sums16[kMaxParts + S - 1] : 0;
+      if (slots > min(a.max_slots, kCutSlots)) break;
       const int ncp = max(1, min(n_ext, items));
       const int waves = (items + ncp - 1) / ncp;
       const float t = waves * (T + kItemCostTiles) + (S > 1 ? kMergeCostTiles : 0.f);
       if (t < best_t * 0.97f) {  // more parts only when they are clearly faster
         best_T = T;
         best_t = t;
+        // the last wave's idle CTAs: as many units take one more part (up to
+        // two more slots each), where that shortens the last wave by clearly
+        // more than an item costs (about T / (S + 1) key tiles)
+        const bool worth = T >= 4.f * kItemCostTiles * (S + 1);
+        best_fill = (waves > 1 && worth) ? min(waves * ncp - items, (a.max_slots - slots) / 2) : 0;
       }
     }
     s_T = best_T;
+    s_fill = best_fill;
   }
   __syncthreads();
   const int T = s_T;
+  const int fill = s_fill;
+  // Filling the last wave: the first `fill` units in unit order that can take
+  // one more part do, so that the items number whole waves; their (smaller)
+  // parts go one size class down, after the others, so the last waves get the
+  // smaller items.  rank0: this thread's count of earlier such units.
+  int rank0 = 0;
+  if (fill > 0) {  // (uniform: the scan's barriers are met by every thread)
+    int elig = 0;
+    for (int u = u_lo; u < u_hi; ++u) {
+      const int n_kv = n_kv_of(u);
+      elig += (unit_parts(n_kv, T) < kMaxParts && n_kv > unit_parts(n_kv, T)) ? 1 : 0;
+    }
+    int elig_total = 0;
+    rank0 = block_exclusive_scan(elig, &elig_total, warp_sums);
+  }
+  // parts of a unit of n_kv key tiles; extra: it took a filling part (rank:
+  // eligible units before it, advanced here)
+  auto parts_of = [&](int n_kv, int& rank, bool& extra) {
+    const int pc = unit_parts(n_kv, T);
+    extra = false;
+    if (fill > 0 && pc < kMaxParts && n_kv > pc) extra = rank++ < fill;
+    return pc + (extra ? 1 : 0);
+  };
   // 3. parts and partial slots per unit (slots in unit order, split units only)
   // (and the cut units' ranks in the list the merge kernel walks)
   int sc2[2] = {0, 0};
-  for (int u = u_lo; u < u_hi; ++u) {
-    const int pc = unit_parts(n_kv_of(u), T);
-    sc2[0] += pc > 1 ? pc : 0;
-    sc2[1] += pc > 1 ? 1 : 0;
+  {
+    int rank = rank0;
+    bool ex;
+    for (int u = u_lo; u < u_hi; ++u) {
+      const int pc = parts_of(n_kv_of(u), rank, ex);
+      sc2[0] += pc > 1 ? pc : 0;
+      sc2[1] += pc > 1 ? 1 : 0;
+    }
   }
   block_scan_n<2>(sc2, reinterpret_cast<int (*)[2]>(&scratch[0][0]), totals);
   int slot = sc2[0], split_rank = sc2[1];
   const int n_split = totals[1];
   if (a.sched_wait && unit_cached) grid_dependency_wait();  // the workspace writes start here
+  int rank = rank0;
+  bool ex;
   for (int u = u_lo; u < u_hi; ++u) {
     const int n_kv = n_kv_of(u);
-    const int pc = unit_parts(n_kv, T);
+    const int pc = parts_of(n_kv, rank, ex);
     UnitEntry e;
     if (unit_cached) {
       int s, pair, g;
@@ -1011,14 +1047,15 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   }
   // item counts per (part, size class); this thread's prefix in each run
   int cnt[kRuns] = {};
+  rank = rank0;
   for (int u = u_lo; u < u_hi; ++u) {
     const int n_kv = n_kv_of(u);
-    const int pc = unit_parts(n_kv, T);
+    const int pc = parts_of(n_kv, rank, ex);
     const int len = (n_kv + pc - 1) / pc;
 #pragma unroll
     for (int p = 0; p < kMaxParts; ++p) {
       const int size = min(len, n_kv - p * len);
-      const int b = size_bucket(max(size, 0), T);
+      const int b = max(0, size_bucket(max(size, 0), T) - (ex ? 1 : 0));
 #pragma unroll
       for (int q = 0; q < kSizeBuckets; ++q) cnt[p * kSizeBuckets + q] += (p < pc && size > 0 && b == q) ? 1 : 0;
     }
@@ -1046,15 +1083,16 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
     const int e0 = last * nc + ((last & 1) ? 0 : rem);
     for (int i = e0 + tid; i < e0 + (nc - rem); i += blockDim.x) a.sched.items[i] = -1;
   }
+  rank = rank0;
   for (int u = u_lo; u < u_hi; ++u) {
     const int n_kv = n_kv_of(u);
-    const int pc = unit_parts(n_kv, T);
+    const int pc = parts_of(n_kv, rank, ex);
     const int len = (n_kv + pc - 1) / pc;
 #pragma unroll
     for (int p = 0; p < kMaxParts; ++p) {
       const int size = min(len, n_kv - p * len);
       if (p >= pc || size <= 0) continue;
-      const int b = size_bucket(size, T);
+      const int b = max(0, size_bucket(size, T) - (ex ? 1 : 0));
       int k = 0;  // this item's position: its run's start plus the items before it in the run
 #pragma unroll
       for (int q = 0; q < kSizeBuckets; ++q)

@@ -24,7 +24,8 @@ constexpr float kItemCostTiles = 3.0f;
 constexpr float kMergeCostTiles = 6.0f;
 constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first order
 constexpr int kItemPartShift = 24;   // item = unit | part << kItemPartShift
-constexpr int kMaxSlots = 1024;      // partial-result slots in the workspace
+constexpr int kMaxSlots = 2048;      // partial-result slots in the workspace
+constexpr int kCutSlots = 1024;      // of which the uniform cut may use (the rest fill the last wave)
 constexpr int kUnitRows = 2 * kBlockM;
 constexpr int kMergeRowGroups = 8;  // merge work items per cut unit (32 rows each)
 constexpr int kMergeThreads = 256;  // merge block: 8 warps, four rows each
