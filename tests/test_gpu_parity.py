@@ -226,6 +226,49 @@ def test_many_short_sequences(cpe):
     np.testing.assert_allclose(lse[rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 
+def test_workspace_rotations_and_two_streams(cpe):
+    """A round's schedule is written before the previous launch finishes only
+    when the previous call on the stream used another workspace.  Rotations
+    A,B,A,B..., A,B,C,A,... and A,A,B,B,... and two requests on two streams
+    (each stream alternating its own pair) all give the bits of the serial
+    run with one workspace."""
+    spec = W.shrink(W.CONFIGS["cfg2"], input_len=2600, chunk=384)
+    _, chunks, ref = _chunked_run(cpe, spec, one_call=True, n_workspaces=1)
+    for n in (2, 3):
+        _, _, out = _chunked_run(cpe, spec, one_call=True, n_workspaces=n)
+        assert torch.equal(out, ref), n
+    # A,A,B,B,...: every other call reuses the previous call's workspace
+    req = W.make_chunked(spec, device="cuda")
+    wss = [cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, "cuda") for _ in range(2)]
+    outs = []
+    for ch in chunks:
+        q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
+        out, _ = cpe.cpe_mixed_step(q, k, v, req.k_cache, req.v_cache, req.page_table, i32([0, ch.query_len]),
+                                    i32([ch.prefix_len]), 0, ch.seq_len, workspace=wss[(ch.index // 2) % 2])
+        outs.append(out)
+    _status_ok(cpe)
+    assert torch.equal(torch.cat(outs), ref)
+    # two requests, one per stream, rounds issued alternately from the host
+    reqs = [W.make_chunked(spec, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wsp = [[cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, "cuda")
+            for _ in range(2)] for _ in range(2)]
+    outs = [[], []]
+    torch.cuda.synchronize()
+    for ch in chunks:
+        for r in range(2):
+            with torch.cuda.stream(streams[r]):
+                q, k, v = reqs[r].round_inputs(ch.prefix_len, ch.query_len)
+                out, _ = cpe.cpe_mixed_step(q, k, v, reqs[r].k_cache, reqs[r].v_cache, reqs[r].page_table,
+                                            i32([0, ch.query_len]), i32([ch.prefix_len]), 0, ch.seq_len,
+                                            workspace=wsp[r][ch.index % 2], stream=streams[r])
+                outs[r].append(out)
+    torch.cuda.synchronize()
+    _status_ok(cpe)
+    for r in range(2):
+        assert torch.equal(torch.cat(outs[r]), ref), r
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def test_cfg2_full(cpe):
