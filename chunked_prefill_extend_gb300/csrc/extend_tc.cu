@@ -13,15 +13,18 @@
 // per row: the article's online-softmax LSE merge, applied tile by tile.
 //
 // Persistent, balanced grid: one CTA per SM.  The schedule kernel lists the
-// units and cuts each into key-range parts of about one target length, chosen
-// so the parts fill whole waves of CTAs (units of equal length get equal
-// parts); it orders the parts largest first in a few size classes, part-major
-// within a class, and deals them to the CTAs in snake order.  CTAs running at
-// the same time then stream the same key range of a KV head (the K/V tiles are
-// read from HBM once and served to the others from L2), and units of unequal
-// length still even out across CTAs.  A unit cut into several parts has each
-// part's normalised partial (O, m, l) written to a workspace slot, and the
-// merge kernel combines them with the same online-softmax LSE rule.
+// units and cuts each into key-range parts of about one target length, the
+// one with the least estimated time (waves of items, each costing its key
+// tiles plus a fixed cost, plus the merge); units of equal length get equal
+// parts, and a last wave left partly idle is filled by giving some units one
+// more, smaller part.  It orders the parts largest first in a few size
+// classes, part-major within a class, and deals them to the CTAs in snake
+// order.  CTAs running at the same time then stream the same key range of a
+// KV head (the K/V tiles are read from HBM once and served to the others from
+// L2), and units of unequal length still even out across CTAs.  A unit cut
+// into several parts has each part's normalised partial (O, m, l) written to
+// a workspace slot, and the merge kernel combines them with the same
+// online-softmax LSE rule.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: both Q tiles of each unit, then the K ring
@@ -34,9 +37,12 @@
 //               O_t += P_t V_j with P read from TMEM, for t = 0, 1 in turn, so
 //               the tensor pipe works on one tile while the other's softmax runs
 //   warps 4-7   softmax of query tile 0, warps 8-11 of query tile 1: one thread
-//               per row reads its S row from TMEM, masks, keeps the running max
-//               (rescaling O only when it grows by more than 2^8), writes P as
-//               bf16 over its S columns, and at the end normalises and stores O.
+//               per row reads its S row from TMEM, masks, takes the
+//               exponentials against the running max (the tile's own max only
+//               when a weight would pass 2^16; the running max then rises only
+//               if the tile's exceeds it by more than 2^8, rescaling O), writes
+//               P as bf16 over its S columns, and at the end normalises and
+//               stores O.
 // The first warpgroup gives registers up (setmaxnreg) to the two softmax
 // warpgroups; the host checks the launch allocation covers the split.
 // TMEM columns: [0,128) S0, [128,256) S1, [256,256+D) O0, [256+D,256+2D) O1.
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const uint32_t tmem = bars->tmem_base;
 
   grid_dependency_wait();    // the schedule (and the round's K/V append) are complete
-  grid_launch_dependents();  // the merge kernels may be scheduled as CTAs finish
+  grid_launch_dependents();  // the merge kernel may be scheduled as CTAs finish
   const int nc = a.sched.header[1];
   const int n_items = a.sched.header[3];  // item-table entries; CTA c takes c, c + nc, ...
   const int cta = blockIdx.x;
