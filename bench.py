@@ -49,20 +49,32 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
+def code_hash(path):
+    """sha256 (first 16 hex digits) of a source file's code: // comments,
+    trailing blanks and empty lines removed, so a comment edit keeps it."""
+    import hashlib
+    import re
+    lines = []
+    for line in open(path, encoding="utf-8").read().splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def profiled_traffic(per_launch_flops):
     """DRAM bytes per extend launch from the committed ncu summary, scaled from
     the captured launch to this one by algorithmic work; None when the kernel
-    source changed since the capture (the counters no longer describe it)."""
-    import hashlib
+    code changed since the capture (the counters no longer describe it)."""
     import re
     try:
-        src = open(os.path.join(ROOT, "chunked_prefill_extend_gb300", "csrc", "extend_tc.cu"), "rb").read()
+        h = code_hash(os.path.join(ROOT, "chunked_prefill_extend_gb300", "csrc", "extend_tc.cu"))
         text = open(os.path.join(ROOT, "profiles", "extend_tc_kernel_cfg5.md")).read()
     except OSError:
         return None
     m = re.search(r"traffic-bytes-per-launch: (\d+) \| captured-launch-flops: (\d+) \| "
-                  r"extend_tc.cu-sha256-16: ([0-9a-f]+)", text)
-    if not m or hashlib.sha256(src).hexdigest()[:16] != m.group(3):
+                  r"extend_tc.cu-code-sha256-16: ([0-9a-f]+)", text)
+    if not m or h != m.group(3):
         return None
     return float(m.group(1)) * per_launch_flops / float(m.group(2))
 
