@@ -138,7 +138,7 @@ Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int m
   L.units_off = 256;
   L.items_off = L.units_off + align256(static_cast<size_t>(cap) * sizeof(UnitEntry));
   L.slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
-  L.split_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(int));
+  L.split_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(ItemDesc));
   L.partial_off = L.split_off + align256(static_cast<size_t>(L.slots / 2 + 1) * sizeof(UnitEntry));
   const size_t parts = static_cast<size_t>(n_seqs) * h_q * L.max_splits;
   L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_bytes(d));
@@ -152,7 +152,7 @@ ExtendSched sched_of(const Layout& L, void* ws) {
   ExtendSched s;
   s.header = reinterpret_cast<int*>(b + L.header_off);
   s.units = reinterpret_cast<UnitEntry*>(b + L.units_off);
-  s.items = reinterpret_cast<int*>(b + L.items_off);
+  s.items = reinterpret_cast<ItemDesc*>(b + L.items_off);
   s.split = reinterpret_cast<UnitEntry*>(b + L.split_off);
   s.partial = b + L.partial_off;
   return s;

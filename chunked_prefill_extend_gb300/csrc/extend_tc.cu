@@ -120,25 +120,24 @@ struct Item {
   __device__ __forceinline__ int n_kt(int t) const { return t ? n_kt_1 : n_kt_0; }
 };
 
-// Fills `it` for item-table entry i; false for an empty entry (or part).
+// Fills `it` for item-table entry i (one descriptor: two independent 16-byte
+// loads); false for an empty entry.
 __device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, Item& it) {
-  const int item = a.sched.items[i];
-  if (item < 0) return false;
-  const int u = item & ((1 << kItemPartShift) - 1);
-  const int p = item >> kItemPartShift;
-  const UnitEntry e = a.sched.units[u];
-  const int len = (e.n_kv + e.parts - 1) / e.parts;
-  it.kv_lo = p * len;
-  it.kv_hi = min(it.kv_lo + len, e.n_kv);
+  const int4* d = reinterpret_cast<const int4*>(a.sched.items + i);
+  const int4 x = d[0];
+  const int4 y = d[1];
+  it.kv_lo = y.y;
+  it.kv_hi = y.z;
   if (it.kv_lo >= it.kv_hi) return false;
-  it.whole = e.parts == 1;
-  it.slot = e.slot + p;
-  it.seq = e.seq;
-  it.g = e.kv_head;
-  it.q0 = a.qo_indptr[e.seq];
-  it.E = a.qo_indptr[e.seq + 1] - it.q0;
-  it.P = a.prefix_len[e.seq];
-  it.i0_0 = 2 * e.pair * a.tok;
+  it.seq = x.x;
+  it.g = x.y >> kPairBits;
+  const int pair = x.y & ((1 << kPairBits) - 1);
+  it.q0 = x.z;
+  it.E = x.w;
+  it.P = y.x;
+  it.slot = y.w;
+  it.whole = it.slot < 0;
+  it.i0_0 = 2 * pair * a.tok;
   it.i0_1 = it.i0_0 + a.tok;
   it.kv_end_0 = it.i0_0 < it.E ? it.P + min(it.E, it.i0_0 + a.tok) : 0;
   it.kv_end_1 = it.i0_1 < it.E ? it.P + min(it.E, it.i0_1 + a.tok) : 0;
@@ -847,7 +846,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   // it: the wait comes before the first workspace write (at once past the
   // shared-memory caches, where the workspace is scratch).
   if (a.sched_wait && !seq_cached) grid_dependency_wait();
-  int* seq_off = seq_cached ? s_seq_off : a.sched.items;
+  int* seq_off = seq_cached ? s_seq_off : reinterpret_cast<int*>(a.sched.items);
   int carry = 0;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     const int k = c0 + tid;
@@ -1087,13 +1086,17 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
     const int last = table_len / nc - 1;
     const int rem = n_items - last * nc;
     const int e0 = last * nc + ((last & 1) ? 0 : rem);
-    for (int i = e0 + tid; i < e0 + (nc - rem); i += blockDim.x) a.sched.items[i] = -1;
+    for (int i = e0 + tid; i < e0 + (nc - rem); i += blockDim.x) a.sched.items[i] = ItemDesc{0, 0, 0, 0, 0, 0, 0, -1};
   }
   rank = rank0;
   for (int u = u_lo; u < u_hi; ++u) {
     const int n_kv = n_kv_of(u);
     const int pc = parts_of(n_kv, rank, ex);
     const int len = (n_kv + pc - 1) / pc;
+    const UnitEntry ue = a.sched.units[u];  // written by this thread above
+    const int q0 = a.qo_indptr[ue.seq];
+    const int E = a.qo_indptr[ue.seq + 1] - q0;
+    const int P = a.prefix_len[ue.seq];
 #pragma unroll
     for (int p = 0; p < kMaxParts; ++p) {
       const int size = min(len, n_kv - p * len);
@@ -1105,7 +1108,8 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
         if (b == q) k = run_start[p * kSizeBuckets + q] + cnt[p * kSizeBuckets + q]++;
       const int wave = k / nc, pos = k - wave * nc;
       const int cta = (wave & 1) ? nc - 1 - pos : pos;
-      a.sched.items[wave * nc + cta] = u | (p << kItemPartShift);
+      a.sched.items[wave * nc + cta] = ItemDesc{ue.seq, (ue.kv_head << kPairBits) | ue.pair, q0, E, P,
+                                                p * len, min(p * len + len, n_kv), pc > 1 ? ue.slot + p : -1};
     }
   }
   if (tid == 0) {

@@ -23,7 +23,7 @@ constexpr int kMaxParts = 8;         // key-range parts a unit may be cut into
 constexpr float kItemCostTiles = 3.0f;
 constexpr float kMergeCostTiles = 6.0f;
 constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first order
-constexpr int kItemPartShift = 24;   // item = unit | part << kItemPartShift
+constexpr int kPairBits = 20;        // ItemDesc::head_pair = kv_head << kPairBits | pair
 constexpr int kMaxSlots = 2048;      // partial-result slots in the workspace
 constexpr int kCutSlots = 1024;      // of which the uniform cut may use (the rest fill the last wave)
 constexpr int kUnitRows = 2 * kBlockM;
@@ -39,17 +39,30 @@ struct UnitEntry {  // one extend work unit: two query tiles of one sequence and
   int slot;      // partial slot of its part 0 (parts > 1); part p uses slot + p
 };
 
+// One entry of the item table: key tiles [kv_lo, kv_hi) of one unit with all a
+// CTA needs to start on it (no further lookups): the sequence, its first row,
+// query length and prefix, the KV head and pair, and the part's partial slot
+// (-1: the unit is not cut; its output goes straight to out / lse).
+// kv_lo >= kv_hi: no item.  Two 16-byte loads.
+struct alignas(16) ItemDesc {
+  int seq;
+  int head_pair;
+  int q0, E, P;
+  int kv_lo, kv_hi;
+  int slot;
+};
+
 // Device-side schedule kept in the caller's workspace.  Unit u is cut into
 // units[u].parts parts; part p covers key tiles [p*len, min((p+1)*len, n_kv))
 // with len = ceil(n_kv / parts).  The item table lists the non-empty parts
-// (unit | part << kItemPartShift, -1 for none); CTA c takes table entries
+// (ItemDesc; empty entries have kv_lo >= kv_hi); CTA c takes table entries
 // c, c + header[1], ...
 struct ExtendSched {
   int* header;          // [0] total key tiles, [1] CTAs used, [2] units, [3] item table length
                         // (a multiple of [1]), [4] target part length, [5] items, [6] next
                         // decode item of a fused mixed step, [7] units cut into parts
   UnitEntry* units;     // [capacity]
-  int* items;           // [item capacity]
+  ItemDesc* items;      // [item capacity]
   uint8_t* partial;     // slots of partial_slot_bytes(d): O [256 x d] bf16 (normalised), then m [256]
                         // (log2) and l [256] fp32
   UnitEntry* split;     // the units cut into parts, in unit order (header[7] of them)
