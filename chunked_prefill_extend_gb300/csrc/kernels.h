@@ -91,10 +91,13 @@ struct DecodeArgs {
 
 // Rates that size the split of a fused mixed step between extend CTAs and
 // decode workers, measured on GB300 at d = 128: one key tile of a two-tile
-// unit takes one SM about 1.97 us alone and about 8 % longer beside decode
+// unit takes one SM about 1.85 us alone and about 8 % longer beside decode
 // rows (they share HBM); decode rows stream K/V at about 55 GB/s per SM, which
-// reaches the 6.67 GB/ms the part sustains at about 120 SMs.
-constexpr float kTileUsPerSm = 1.97f;
+// reaches the 6.67 GB/ms the part sustains at about 120 SMs.  (Swept forced
+// splits put the best step at 44 extend CTAs for 256 decode rows beside a
+// 2048-token chunk at prefix 30720, and at 128 for the scheduled step with 64
+// decode rows and four chunks: the rule picks both.)
+constexpr float kTileUsPerSm = 1.85f;
 constexpr float kFusedExtendSlowdown = 1.08f;
 constexpr float kDecodeBytesPerUs = 6.67e6f;
 constexpr int kDecodeSatSms = 120;
