@@ -21,7 +21,7 @@ constexpr int kMaxParts = 8;         // key-range parts a unit may be cut into
 // merge of units cut into parts (the partial results' writes and the merge
 // launch after the extend launch has drained).
 constexpr float kItemCostTiles = 3.0f;
-constexpr float kMergeCostTiles = 6.0f;
+constexpr float kMergeCostTiles = 4.0f;
 constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first order
 constexpr int kPairBits = 20;        // ItemDesc::head_pair = kv_head << kPairBits | pair
 constexpr int kMaxSlots = 2048;      // partial-result slots in the workspace
