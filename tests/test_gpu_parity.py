@@ -322,6 +322,34 @@ def test_cfg5_sampled(cpe):
     assert len(chunks) == 128 and chunks[-1].seq_len == 131072
 
 
+def test_d64_long_rounds_cut_units_sampled(cpe):
+    """d = 64 with rounds long enough that the schedule cuts every unit into
+    four or five key-range parts and fills the last wave, so the merge
+    kernel's d = 64 path (one bf16 pair per lane) combines them; sampled rows
+    against the oracle."""
+    spec = W.shrink(W.CONFIGS["cfg5"], name="d64", input_len=32768, chunk=2048, h_q=32, h_kv=4, d=64)
+    chunks = _sampled_rounds(cpe, spec, [0, 7], 32, 700)
+    # the last round again, with a workspace whose schedule header can be read:
+    # header[7] counts the units cut into parts
+    req = W.make_chunked(spec, device="cuda")
+    for ch in chunks:
+        q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
+        cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, i32([0, ch.query_len]),
+                          i32([ch.prefix_len]))
+    ch = chunks[-1]
+    q, _, _ = req.round_inputs(ch.prefix_len, ch.query_len)
+    ws = cpe.alloc_workspace(1, ch.query_len, spec.h_q, spec.h_kv, spec.d, ch.seq_len, "cuda")
+    out, _ = cpe.cpe_extend_attention(q, req.k_cache, req.v_cache, req.page_table, i32([0, ch.query_len]),
+                                      i32([ch.prefix_len]), ch.seq_len, workspace=ws)
+    _status_ok(cpe)
+    assert int(ws[:32].view(torch.int32)[7]) > 0
+    rows = W.sample_rows(ch.query_len, 128 // (spec.h_q // spec.h_kv), 32, 715)
+    ref_o, _ = oracle.extend_attention(q.cpu(), req.k_cache.cpu(), req.v_cache.cpu(),
+                                       torch.tensor([req.page_table_host], dtype=torch.int32),
+                                       [0, ch.query_len], [ch.prefix_len], spec.h_q, spec.h_kv, rows=rows)
+    check_close(out[rows], ref_o, "d64 last round, cut units")
+
+
 # ---------------------------------------------------------------- decode rows
 
 @pytest.mark.parametrize("lens", [[1, 2, 15, 16, 17, 100], [2047, 2048, 2049, 4096, 4097, 9000], [32768, 1, 513]])
