@@ -1,14 +1,14 @@
 #!/usr/bin/env python3
 """Benchmark of chunked-prefill extend attention on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg5] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill-128k-c1024] [--impl ours|reference]
 
 A step is one pass of the hot path over one batch of synthetic input:
-  cfg1/2/3/5  the whole chunked prefill of one request: the chunk plan, then
+  fp32-512, prefill-*   the whole chunked prefill of one request: the chunk plan, then
               for every chunk the KV append and the extend attention;
-  cfg4        one mixed step: the mixed-step plan, the KV append, the
+  mixed-256dec-2048     one mixed step: the mixed-step plan, the KV append, the
               split-KV decode rows and the prefill chunk.
-Default workload: cfg5 (N=131072, C=1024, 128 chunks, GQA 64/8, d=128, bf16),
+Default workload: prefill-128k-c1024 (N=131072, C=1024, 128 chunks, GQA 64/8, d=128, bf16),
 the long-context configuration whose per-chunk TFLOP/s the metric tracks.
 
 Rank 0 prints one JSON line.  ``value`` is algorithmic TFLOP/s over all ranks
@@ -69,7 +69,7 @@ def profiled_traffic(per_launch_flops):
     import re
     try:
         h = code_hash(os.path.join(ROOT, "chunked_prefill_extend_gb300", "csrc", "extend_tc.cu"))
-        text = open(os.path.join(ROOT, "profiles", "extend_tc_kernel_cfg5.md")).read()
+        text = open(os.path.join(ROOT, "profiles", "extend_tc_kernel_prefill-128k-c1024.md")).read()
     except OSError:
         return None
     m = re.search(r"traffic-bytes-per-launch: (\d+) \| captured-launch-flops: (\d+) \| "
@@ -86,7 +86,7 @@ def chunk_flops(d, h_q, P, E):
 # --------------------------------------------------------------------------- workloads
 
 class Chunked:
-    """Whole chunked prefill of one request (cfg1/2/3/5)."""
+    """Whole chunked prefill of one request."""
 
     def __init__(self, spec, device, cpe, rounds=None):
         self.spec, self.cpe, self.device = spec, cpe, device
@@ -244,7 +244,7 @@ class Chunked:
 
 
 class Mixed:
-    """One mixed step (cfg4)."""
+    """One mixed step: decode rows and one prefill chunk under one token budget."""
 
     def __init__(self, spec, device, cpe):
         self.spec, self.cpe, self.device = spec, cpe, device
@@ -585,7 +585,7 @@ def run_ours(args, ws, rank, local):
         achieved = per_launch / (kms * 1e-3) / 1e12
         pk = peaks["bf16_sustained"]
         traffic = (profiled_traffic(per_launch)
-                   if args.workload == "cfg5" and not args.input_len and not args.rounds else None)
+                   if args.workload == "prefill-128k-c1024" and not args.input_len and not args.rounds else None)
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
                 "traffic": traffic,
                 "kernel": "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)",
@@ -792,7 +792,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="cfg5", choices=sorted(W.CONFIGS))
+    ap.add_argument("--workload", default="prefill-128k-c1024", choices=sorted(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")

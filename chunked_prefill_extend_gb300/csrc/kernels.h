@@ -187,7 +187,7 @@ cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream
 // The extend launch + the merge of split units.  `dependent`: launch both with
 // programmatic stream serialisation (each may be scheduled while the kernel
 // before it finishes), which hides launch latency on short launches; on long
-// ones (measured on cfg5's 1.7 ms launches) it costs about 1 %, so the caller
+// ones (measured on the 128k-token request's 1.7 ms rounds) it costs about 1 %, so the caller
 // turns it on only below kDependentLaunchFlops of extend work.
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent);
 constexpr double kDependentLaunchFlops = 2e11;

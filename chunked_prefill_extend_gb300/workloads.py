@@ -8,14 +8,14 @@ fixed order of draws.
 
 Workloads (shapes of the pages' long-context chunked prefill):
 
-``cfg1``  one request N=512, chunk 128, 4/4 heads, d=64, fp32 N(0,1), contiguous cache
-``cfg2``  one request N=4000, chunk 512, 32/8 heads, d=128, bf16 N(0,1)*0.5, page 16
-``cfg3``  input 32768 with 50% prefix-cache hit: 16384 cached tokens N(0,1), two
+``fp32-512``  one request N=512, chunk 128, 4/4 heads, d=64, fp32 N(0,1), contiguous cache
+``prefill-4000-c512``  one request N=4000, chunk 512, 32/8 heads, d=128, bf16 N(0,1)*0.5, page 16
+``prefill-32k-hit50``  input 32768 with 50% prefix-cache hit: 16384 cached tokens N(0,1), two
           extend rounds of 8192, 32/8, d=128, bf16 N(0,1)*0.5 for the extend part
-``cfg4``  mixed step, budget 2304: one prefill chunk at prefix 30720 plus 256
+``mixed-256dec-2048``  mixed step, budget 2304: one prefill chunk at prefix 30720 plus 256
           decode rows with context lengths uniform on {512..32768}, 32/8, d=128,
           bf16 N(0,1)*0.5, all pages drawn from one pool in a random permutation
-``cfg5``  one request N=131072, chunk 1024 (128 rounds), 64/8, d=128, bf16 N(0,1)*0.5
+``prefill-128k-c1024``  one request N=131072, chunk 1024 (128 rounds), 64/8, d=128, bf16 N(0,1)*0.5
 """
 from __future__ import annotations
 
@@ -85,22 +85,22 @@ class ScheduledSpec:
 
 
 CONFIGS = {
-    "cfg1": ChunkedSpec("cfg1", 1, 512, 0.0, 128, 4, 4, 64, torch.float32, std=1.0, prefix_std=1.0),
-    "cfg2": ChunkedSpec("cfg2", 2, 4000, 0.0, 512, 32, 8, 128, torch.bfloat16),
-    "cfg3": ChunkedSpec("cfg3", 3, 32768, 0.5, 8192, 32, 8, 128, torch.bfloat16, prefix_std=1.0),
-    "cfg4": MixedSpec("cfg4", 4, 2304, 256, 512, 32768, 30720, 4096, 32, 8, 128, torch.bfloat16),
-    "cfg5": ChunkedSpec("cfg5", 5, 131072, 0.0, 1024, 64, 8, 128, torch.bfloat16),
+    "fp32-512": ChunkedSpec("fp32-512", 1, 512, 0.0, 128, 4, 4, 64, torch.float32, std=1.0, prefix_std=1.0),
+    "prefill-4000-c512": ChunkedSpec("prefill-4000-c512", 2, 4000, 0.0, 512, 32, 8, 128, torch.bfloat16),
+    "prefill-32k-hit50": ChunkedSpec("prefill-32k-hit50", 3, 32768, 0.5, 8192, 32, 8, 128, torch.bfloat16, prefix_std=1.0),
+    "mixed-256dec-2048": MixedSpec("mixed-256dec-2048", 4, 2304, 256, 512, 32768, 30720, 4096, 32, 8, 128, torch.bfloat16),
+    "prefill-128k-c1024": ChunkedSpec("prefill-128k-c1024", 5, 131072, 0.0, 1024, 64, 8, 128, torch.bfloat16),
     "sched": ScheduledSpec("sched", 6, 8192, 64, 512, 32768, ((8192, 2048), (30720, 2048), (65536, 2048)),
                            ((4096, 16384), (0, 4000)), 32, 8, 128, torch.bfloat16),
 }
 
 WORKLOAD_TEXT = {
-    "cfg1": "one request N=512, chunk 128, 4/4 heads, d=64, fp32, contiguous cache",
-    "cfg2": "one request N=4000, chunk 512 (7x512+416), GQA 32/8, d=128, bf16, page 16",
-    "cfg3": "input 32768, 50% prefix hit (16384 cached), 2 chunks of 8192, GQA 32/8, d=128, bf16",
-    "cfg4": "mixed step budget 2304: prefill E=2048 at P=30720 + 256 decode rows L~U[512,32768], "
+    "fp32-512": "one request N=512, chunk 128, 4/4 heads, d=64, fp32, contiguous cache",
+    "prefill-4000-c512": "one request N=4000, chunk 512 (7x512+416), GQA 32/8, d=128, bf16, page 16",
+    "prefill-32k-hit50": "input 32768, 50% prefix hit (16384 cached), 2 chunks of 8192, GQA 32/8, d=128, bf16",
+    "mixed-256dec-2048": "mixed step budget 2304: prefill E=2048 at P=30720 + 256 decode rows L~U[512,32768], "
             "GQA 32/8, d=128, bf16, permuted pages",
-    "cfg5": "one request N=131072, chunk 1024 (128 chunks), GQA 64/8, d=128, bf16, page 16",
+    "prefill-128k-c1024": "one request N=131072, chunk 1024 (128 chunks), GQA 64/8, d=128, bf16, page 16",
     "sched": "one scheduling step, budget 8192: 64 decode rows L~U[512,32768], running prefills at "
              "P=8192/30720/65536 (2048 tokens each), waiting prompts 16384 (4096 cached, cut to 1984) and 4000 "
              "(left queued); GQA 32/8, d=128, bf16, permuted pages",

@@ -100,7 +100,7 @@ def test_plan_schedule_errors():
             cpe.cpe_plan_schedule(budget, running, waiting)
 
 
-def test_mixed_step_cfg4_shape():
+def test_mixed_step_budget_2304_shape():
     out = cpe.cpe_plan_mixed_step(2304, [1000] * 256, 30720, 4096)
     assert out["extend_len"] == 2048 and out["n_decode"] == 256 and out["qo_indptr"][-1] == 2304
 

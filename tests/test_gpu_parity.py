@@ -139,20 +139,20 @@ def _chunked_run(cpe, spec, device="cuda", one_call=False, n_workspaces=0):
     return req, chunks, torch.cat(outs)
 
 
-def test_cfg1_chunked_equals_one_shot_fp32(cpe):
-    spec = W.CONFIGS["cfg1"]
+def test_fp32_512_chunked_equals_one_shot(cpe):
+    spec = W.CONFIGS["fp32-512"]
     req, chunks, out = _chunked_run(cpe, spec)
     assert [c.query_len for c in chunks] == [128] * 4
     one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
-    check_close(out, one, "cfg1 chunked vs one-shot", max_abs=1e-4, rel_rms=1e-5)
+    check_close(out, one, "fp32-512 chunked vs one-shot", max_abs=1e-4, rel_rms=1e-5)
     # the GPU's own one-shot run (one chunk of 512) agrees with its chunked run
     spec1 = W.shrink(spec, chunk=512)
     _, _, out1 = _chunked_run(cpe, spec1)
-    check_close(out, out1.double().cpu().numpy(), "cfg1 gpu chunked vs gpu one-shot", max_abs=1e-4, rel_rms=1e-5)
+    check_close(out, out1.double().cpu().numpy(), "fp32-512 gpu chunked vs gpu one-shot", max_abs=1e-4, rel_rms=1e-5)
 
 
 def test_bf16_chunked_equals_one_shot(cpe):
-    spec = W.shrink(W.CONFIGS["cfg2"], input_len=1500, chunk=256)
+    spec = W.shrink(W.CONFIGS["prefill-4000-c512"], input_len=1500, chunk=256)
     req, _, out = _chunked_run(cpe, spec)
     one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
     check_close(out, one, "bf16 chunked vs one-shot")
@@ -232,7 +232,7 @@ def test_workspace_rotations_and_two_streams(cpe):
     A,B,A,B..., A,B,C,A,... and A,A,B,B,... and two requests on two streams
     (each stream alternating its own pair) all give the bits of the serial
     run with one workspace."""
-    spec = W.shrink(W.CONFIGS["cfg2"], input_len=2600, chunk=384)
+    spec = W.shrink(W.CONFIGS["prefill-4000-c512"], input_len=2600, chunk=384)
     _, chunks, ref = _chunked_run(cpe, spec, one_call=True, n_workspaces=1)
     for n in (2, 3):
         _, _, out = _chunked_run(cpe, spec, one_call=True, n_workspaces=n)
@@ -271,15 +271,15 @@ def test_workspace_rotations_and_two_streams(cpe):
 
 # ---------------------------------------------------------------- full-size workloads
 
-def test_cfg2_full(cpe):
-    """Every row of cfg2, each round in one call as the benchmark runs it (two
+def test_prefill_4000_c512_full(cpe):
+    """Every row of prefill-4000-c512, each round in one call as the benchmark runs it (two
     workspaces alternated, so a round's tile list is written while the previous
     round runs); one shared workspace gives the same bits."""
-    spec = W.CONFIGS["cfg2"]
+    spec = W.CONFIGS["prefill-4000-c512"]
     req, chunks, out = _chunked_run(cpe, spec, one_call=True, n_workspaces=2)
     assert [c.query_len for c in chunks] == [512] * 7 + [416]
     one, _ = oracle.causal_attention(req.q.cpu(), req.k.cpu(), req.v.cpu(), spec.h_q, spec.h_kv)
-    check_close(out, one, "cfg2 all rows")
+    check_close(out, one, "prefill-4000-c512 all rows")
     _, _, out1 = _chunked_run(cpe, spec, one_call=True, n_workspaces=1)
     assert torch.equal(out, out1)
     # the separate append + extend calls, alternating too
@@ -312,13 +312,13 @@ def _sampled_rounds(cpe, spec, round_ids, n_rows, seed):
     return chunks
 
 
-def test_cfg3_sampled(cpe):
-    chunks = _sampled_rounds(cpe, W.CONFIGS["cfg3"], [0, 1], 96, 300)
+def test_prefill_32k_hit50_sampled(cpe):
+    chunks = _sampled_rounds(cpe, W.CONFIGS["prefill-32k-hit50"], [0, 1], 96, 300)
     assert [(c.prefix_len, c.query_len) for c in chunks] == [(16384, 8192), (24576, 8192)]
 
 
-def test_cfg5_sampled(cpe):
-    chunks = _sampled_rounds(cpe, W.CONFIGS["cfg5"], [0, 7, 127], 24, 500)
+def test_prefill_128k_c1024_sampled(cpe):
+    chunks = _sampled_rounds(cpe, W.CONFIGS["prefill-128k-c1024"], [0, 7, 127], 24, 500)
     assert len(chunks) == 128 and chunks[-1].seq_len == 131072
 
 
@@ -327,7 +327,7 @@ def test_d64_long_rounds_cut_units_sampled(cpe):
     four or five key-range parts and fills the last wave, so the merge
     kernel's d = 64 path (one bf16 pair per lane) combines them; sampled rows
     against the oracle."""
-    spec = W.shrink(W.CONFIGS["cfg5"], name="d64", input_len=32768, chunk=2048, h_q=32, h_kv=4, d=64)
+    spec = W.shrink(W.CONFIGS["prefill-128k-c1024"], name="d64", input_len=32768, chunk=2048, h_q=32, h_kv=4, d=64)
     chunks = _sampled_rounds(cpe, spec, [0, 7], 32, 700)
     # the last round again, with a workspace whose schedule header can be read:
     # header[7] counts the units cut into parts
@@ -400,8 +400,8 @@ def test_mixed_step_fused_shapes_full(cpe, h_q, h_kv, d):
     np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 
-def test_cfg4_mixed_sampled(cpe):
-    spec = W.CONFIGS["cfg4"]
+def test_mixed_256dec_2048_sampled(cpe):
+    spec = W.CONFIGS["mixed-256dec-2048"]
     g = torch.Generator().manual_seed(spec.seed)
     ctx = torch.randint(spec.ctx_lo, spec.ctx_hi + 1, (spec.n_decode,), generator=g).tolist()
     plan = cpe.cpe_plan_mixed_step(spec.token_budget, ctx, spec.prefill_prefix, spec.prefill_remaining)
@@ -421,7 +421,7 @@ def test_cfg4_mixed_sampled(cpe):
     q = mb.q[dec].cpu()
     ref_o, ref_l = oracle.extend_attention(q, kc, vc, pt, list(range(len(dec) + 1)),
                                            [plan["prefix_len"][s] for s in dec], spec.h_q, spec.h_kv)
-    check_close(out[dec], ref_o, "cfg4 decode rows")
+    check_close(out[dec], ref_o, "mixed-256dec-2048 decode rows")
     np.testing.assert_allclose(lse[dec].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
     # prefill rows
     ps = 256
@@ -430,7 +430,7 @@ def test_cfg4_mixed_sampled(cpe):
     q = mb.q[256:]
     ref_o, ref_l = oracle.extend_attention(q.cpu(), kc, vc, pt, [0, 2048], [plan["prefix_len"][ps]], spec.h_q,
                                            spec.h_kv, rows=rows)
-    check_close(out[256:][rows], ref_o, "cfg4 prefill rows")
+    check_close(out[256:][rows], ref_o, "mixed-256dec-2048 prefill rows")
     np.testing.assert_allclose(lse[256:][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 

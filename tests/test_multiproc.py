@@ -50,7 +50,7 @@ def test_reference_arm_prints_one_line_from_rank0_only():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
-           "--impl", "reference", "--workload", "cfg4", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+           "--impl", "reference", "--workload", "mixed-256dec-2048", "--gpus", "2", "--steps", "1", "--warmup", "0"]
     env = dict(os.environ, OMP_NUM_THREADS="2")
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]

@@ -132,10 +132,10 @@ def test_dominant_key_selects_its_value():
         np.testing.assert_allclose(out[i, 0], vc[page, slot, 0].double().numpy(), atol=1e-9)
 
 
-def test_chunked_equals_one_shot_cfg1():
+def test_chunked_equals_one_shot_fp32_512():
     """The article's exactness claim on the fp32 workload: four 128-token
     extend rounds through the paged cache equal one-shot causal prefill."""
-    spec = W.CONFIGS["cfg1"]
+    spec = W.CONFIGS["fp32-512"]
     req = W.make_chunked(spec)
     one, one_lse = oracle.causal_attention(req.q, req.k, req.v, spec.h_q, spec.h_kv)
     outs, lses = [], []
@@ -152,7 +152,7 @@ def test_chunked_equals_one_shot_cfg1():
 
 
 def test_chunked_equals_one_shot_gqa_bf16():
-    spec = W.shrink(W.CONFIGS["cfg2"], input_len=300, chunk=64, h_q=8, h_kv=2, d=32, page_perm=True)
+    spec = W.shrink(W.CONFIGS["prefill-4000-c512"], input_len=300, chunk=64, h_q=8, h_kv=2, d=32, page_perm=True)
     req = W.make_chunked(spec)
     one, _ = oracle.causal_attention(req.q, req.k, req.v, spec.h_q, spec.h_kv)
     outs = []
