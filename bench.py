@@ -90,8 +90,8 @@ class Chunked:
 
     def __init__(self, spec, device, cpe, rounds=None):
         self.spec, self.cpe, self.device = spec, cpe, device
-        self.req = W.make_chunked(spec, device=device)
         self.chunks, self.cached, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+        self.req = W.make_chunked(spec, self.cached, device=device)
         self.rounds = rounds or (0, len(self.chunks))
         if self.rounds[0] > 0:  # the cache must hold every earlier round's keys
             for c in self.chunks[:self.rounds[0]]:
@@ -115,7 +115,7 @@ class Chunked:
         self.in_bytes = sum(t.numel() * t.element_size() for t in (self.req.q, self.req.k, self.req.v))
         self.kernel = "extend_tc_kernel" if spec.dtype == torch.bfloat16 else "extend_simt_kernel"
         self.bound = "tensor"
-        self.small = self.in_bytes + 2 * self.req.k_cache.numel() * self.req.k_cache.element_size() < 2 * L2_BYTES
+        self.small = l2_text(spec).startswith("flushed")
 
     def chunk_call(self, c, q, k, v, out):
         """One round: its K/V appended and its extend attention, in one call
@@ -492,25 +492,45 @@ def flush_l2(buf):
 
 # --------------------------------------------------------------------------- arms
 
-def run_ours(args, ws, rank, local):
+def l2_text(spec):
+    """How the timed steps keep L2 from serving a step's inputs from the one
+    before: chunked workloads whose inputs and caches fit twice in L2 are
+    flushed between steps, everything else is larger than L2."""
+    if isinstance(spec, W.ChunkedSpec):
+        es = 2 if spec.dtype == torch.bfloat16 else 4
+        n_new = spec.input_len - math.floor(spec.input_len * spec.hit_rate)
+        pages = -(-spec.input_len // spec.page_size)
+        b = n_new * (spec.h_q + 2 * spec.h_kv) * spec.d * es + 2 * pages * spec.page_size * spec.h_kv * spec.d * es
+        if b < 2 * L2_BYTES:
+            return "flushed between steps (256 MiB write outside the per-step events)"
+    return "inputs larger than L2 (no flush)"
+
+
+def workload_config(name, args, ws):
+    return {"workload": f"{name}: {W.WORKLOAD_TEXT[name]}" +
+            (f" (input_len {args.input_len})" if args.input_len else "") +
+            (f" (decode rows {args.decode_rows})" if args.decode_rows else "") +
+            (f" (rounds {args.rounds})" if args.rounds else ""),
+            "l2": l2_text(W.CONFIGS[name]), "parallelism": f"replicas x{ws}"}
+
+
+def measure(wl, name, steps, warmup, peaks, ws, device, traffic_ok=False):
+    """Warm-up, then `steps` timed steps of workload `wl` (events around each
+    step, clocks sampled meanwhile), then its dominant kernel's roofline.
+    Returns the fields of a bench line for this workload."""
     from chunked_prefill_extend_gb300 import cpe
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    peaks = _peaks()
-    wl = make_workload(args, device, cpe)
     flush = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if wl.small else None
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         wl.step()
         if flush is not None:
             flush_l2(flush)
     st, detail = cpe.cpe_get_device_status()
     if st != cpe.CPE_OK:
-        raise RuntimeError(f"device status after warm-up: {cpe.cpe_status_string(st)} ({detail})")
+        raise RuntimeError(f"{name}: device status after warm-up: {cpe.cpe_status_string(st)} ({detail})")
 
-    clocks = Clocks(local)
+    clocks = Clocks(device.index or 0)
     clocks.start()
     time.sleep(0.3)
-    kev = ([], [])
     sev = []
     launches0 = cpe.cpe_launch_count()
     barrier(ws)
@@ -518,7 +538,7 @@ def run_ours(args, ws, rank, local):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -534,18 +554,18 @@ def run_ours(args, ws, rank, local):
     clk = clocks.stop()
     st, detail = cpe.cpe_get_device_status()
     if st != cpe.CPE_OK:
-        raise RuntimeError(f"device status after timing: {cpe.cpe_status_string(st)} ({detail})")
+        raise RuntimeError(f"{name}: device status after timing: {cpe.cpe_status_string(st)} ({detail})")
     step_ms = [a.elapsed_time(b) for a, b in sev]
     region_ms = t_start.elapsed_time(t_end)
     my_ms = sum(step_ms) if flush is not None else region_ms
     total_ms = max_over_ranks(my_ms, ws, device)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / steps
     value = wl.flops * ws / (ms_per_step * 1e-3) / 1e12
 
     # dominant kernel, timed live with events on the launching stream
     if isinstance(wl, Scheduled):
         ext_ev, dev_ev = ([], []), ([], [])
-        for _ in range(max(3, args.steps // 2)):
+        for _ in range(max(3, steps // 2)):
             wl.extend_only(ext_ev)
             wl.decode_only(dev_ev)
         torch.cuda.synchronize()
@@ -553,17 +573,18 @@ def run_ours(args, ws, rank, local):
         dms = statistics.mean(a.elapsed_time(b) for a, b in zip(*dev_ev))
         achieved = wl.extend_flops / (kms * 1e-3) / 1e12
         pk = peaks["bf16_sustained"]
+        dach = wl.decode_bytes / (dms * 1e-3) / 1e9
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
                 "traffic": None, "kernel": "extend attention call on the step's prefill chunks",
                 "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": wl.extend_flops,
-                "decode_rows": {"achieved": wl.decode_bytes / (dms * 1e-3) / 1e9, "unit": "GB/s",
-                                "peak": peaks["hbm_gbs"], "ms": dms},
+                "decode_rows": {"achieved": dach, "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                                "frac": dach / peaks["hbm_gbs"], "ms": dms},
                 "per_chunk": [{"prefix_len": P, "query_len": E} for P, E in wl.lens[wl.plan["n_decode"]:]]}
     elif isinstance(wl, Mixed):
         # the step is one fused launch (decode rows on the CTAs the prefill
         # chunk leaves free); its HBM roofline counts the K/V it must read
         dev_ev = ([], [])
-        for _ in range(max(3, args.steps // 2)):
+        for _ in range(max(3, steps // 2)):
             wl.decode_only(dev_ev)
         torch.cuda.synchronize()
         dms = statistics.mean(a.elapsed_time(b) for a, b in zip(*dev_ev))
@@ -583,16 +604,19 @@ def run_ours(args, ws, rank, local):
         kms = ms_per_step / nch
         per_launch = wl.flops / nch
         achieved = per_launch / (kms * 1e-3) / 1e12
-        pk = peaks["bf16_sustained"]
-        traffic = (profiled_traffic(per_launch)
-                   if args.workload == "prefill-128k-c1024" and not args.input_len and not args.rounds else None)
+        if wl.spec.dtype == torch.bfloat16:
+            pk, src = peaks["bf16_sustained"], peaks["source"] + " bf16_tflops_sustained"
+        else:  # tf32 tensor cores: half the bf16 rate per the nominal dense figures (1.1 vs 2.25 PFLOP/s)
+            pk, src = peaks["bf16_sustained"] / 2, peaks["source"] + " bf16_tflops_sustained x 1/2 (tf32)"
+        traffic = profiled_traffic(per_launch) if traffic_ok else None
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
                 "traffic": traffic,
                 "kernel": "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)",
-                "peak_source": peaks["source"] + " bf16_tflops_sustained", "units_per_launch": per_launch}
+                "peak_source": src, "units_per_launch": per_launch}
         # per round: a pass after the timed region with events around every
         # call (so each call runs alone); the median over its steps
-        for _ in range(args.steps):
+        kev = ([], [])
+        for _ in range(steps):
             wl.step(ev=kev)
             if flush is not None:
                 flush_l2(flush)
@@ -601,31 +625,58 @@ def run_ours(args, ws, rank, local):
         med = [statistics.median(kms_list[i::nch]) for i in range(nch)]
         curve = [(c.prefix_len, chunk_flops(wl.spec.d, wl.spec.h_q, c.prefix_len, c.query_len) / (t * 1e-3) / 1e12)
                  for c, t in zip(wl.chunks, med)]
-        pick = sorted(set([0, len(curve) // 4, len(curve) // 2, 3 * len(curve) // 4, len(curve) - 1]))
+        pick = sorted(set([0, len(curve) // 4, len(curve) // 2, 3 * len(curve) // 4, len(curve) - 1])) \
+            if len(curve) > 8 else list(range(len(curve)))
         roof["per_chunk_tflops"] = {str(curve[i][0]): round(curve[i][1], 1) for i in pick}
         roof["per_chunk_reps"] = len(kms_list) // nch
         roof["aggregate_tflops"] = wl.flops / (sum(med) * 1e-3) / 1e12  # sum of flops / sum of median times
+    return {"value": value, "ms_per_step": ms_per_step, "tokens_per_s": wl.tokens * ws / (ms_per_step * 1e-3),
+            "flops_per_step": wl.flops, "roofline": roof, "clocks": clk, "gpu_launches": launches,
+            "steps": steps, "warmup": warmup}
+
+
+# the other workloads, timed after the headline in the same run
+PER_CONFIG = ("prefill-4000-c512", "prefill-32k-hit50", "mixed-256dec-2048", "sched", "fp32-512")
+
+
+def run_ours(args, ws, rank, local):
+    from chunked_prefill_extend_gb300 import cpe
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks = _peaks()
+    wl = make_workload(args, device, cpe)
+    full = not args.input_len and not args.rounds and not args.decode_rows
+    m = measure(wl, args.workload, args.steps, args.warmup, peaks, ws, device,
+                traffic_ok=args.workload == "prefill-128k-c1024" and full)
 
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else e2e_measure(wl, args, device, ws)
 
     line = {
         "metric": "extend-attn TFLOP/s & tokens/s per chunk; % bf16 TC peak / % HBM BW (1 GB300)",
-        "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "value": m["value"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if W.CONFIGS[args.workload].dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "tokens_per_s": wl.tokens * ws / (ms_per_step * 1e-3),
-        "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}" +
-                   (f" (input_len {args.input_len})" if args.input_len else "") +
-                   (f" (decode rows {args.decode_rows})" if args.decode_rows else "") +
-                   (f" (rounds {args.rounds})" if args.rounds else ""),
-                   "l2": "flushed between steps (256 MiB write outside the per-step events)" if flush is not None
-                   else "inputs larger than L2 (no flush)",
-                   "parallelism": f"replicas x{ws}", "flops_per_step": wl.flops},
-        "roofline": roof, "clocks": clk, "gpu_launches": launches, "e2e": e2e,
+        "tokens_per_s": m["tokens_per_s"], "flops_per_step": m["flops_per_step"],
+        "config": workload_config(args.workload, args, ws),
+        "roofline": m["roofline"], "clocks": m["clocks"], "gpu_launches": m["gpu_launches"], "e2e": e2e,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args)
+    if full and args.workload == "prefill-128k-c1024" and not args.no_per_config:
+        del wl
+        torch.cuda.empty_cache()
+        per = {}
+        for name in PER_CONFIG:
+            a2 = argparse.Namespace(**{**vars(args), "workload": name})
+            w2 = make_workload(a2, device, cpe)
+            r = measure(w2, name, 20, 5, peaks, ws, device)
+            r["config"] = workload_config(name, a2, ws)
+            r["dtype"] = "bf16" if W.CONFIGS[name].dtype == torch.bfloat16 else "f32"
+            per[name] = r
+            del w2
+            torch.cuda.empty_cache()
+        line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -728,7 +779,7 @@ def run_reference(args, ws, rank, local):
             "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{args.workload}: {W.WORKLOAD_TEXT[args.workload]}"},
+            "config": workload_config(args.workload, args, ws),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": wl.text},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -796,6 +847,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads timed after the default one")
     ap.add_argument("--input-len", type=int, default=0, help="shrink a chunked workload's request (profiling)")
     ap.add_argument("--decode-rows", type=int, default=0, help="shrink the mixed step's decode rows (profiling)")
     ap.add_argument("--rounds", default="", help="a:b, run only chunks [a, b) of a chunked workload (profiling)")

@@ -19,7 +19,6 @@ Workloads (shapes of the pages' long-context chunked prefill):
 """
 from __future__ import annotations
 
-import math
 from dataclasses import dataclass, field, replace
 
 import torch
@@ -149,16 +148,18 @@ class ChunkedRequest:
         return self.q[a:a + query_len], self.k[a:a + query_len], self.v[a:a + query_len]
 
 
-def make_chunked(spec: ChunkedSpec, device="cpu", prefill_cache: bool = True) -> ChunkedRequest:
+def make_chunked(spec: ChunkedSpec, cached: int, device="cpu", prefill_cache: bool = True) -> ChunkedRequest:
     """Draw the request: pre-filled prefix K/V, extend-part Q/K/V, pages.
 
-    The cached prefix (floor(input_len * hit_rate) tokens, the pages' rule) is
-    written straight into its pages here, the way an earlier request would
-    have left it; its K/V values are not kept elsewhere.
+    ``cached`` is the prefix-cache hit the caller's chunk plan reports (the
+    first chunk's prefix length); those tokens' K/V are written straight into
+    their pages here, the way an earlier request would have left them, and are
+    not kept elsewhere.
     """
+    if not 0 <= cached < spec.input_len:
+        raise ValueError("cached must be in [0, input_len)")
     gen = torch.Generator(device=device)
     gen.manual_seed(spec.seed)
-    cached = math.floor(spec.input_len * spec.hit_rate)
     n_new = spec.input_len - cached
     num_pages = _pages(spec.input_len, spec.page_size)
     if spec.page_perm:

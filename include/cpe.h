@@ -22,7 +22,10 @@
  *    available from cpe_last_error() on the calling thread.  Errors found on
  *    the device (a page id out of range, a length above max_kv_len, a pipeline
  *    wait that gave up) are recorded in a device status word that
- *    cpe_get_device_status() reads and clears.
+ *    cpe_get_device_status() reads and clears.  The library looks up the
+ *    word's device address once per device and keeps it, so a
+ *    cudaDeviceReset in the process voids it: use the library on a device
+ *    only while the context of its first call there is alive.
  *  - Layouts are row-major with the last dimension contiguous:
  *      q, out       [total_q, H_q, d]
  *      k_new, v_new [total_q, H_kv, d]
@@ -348,7 +351,9 @@ cpe_status cpe_decode_attention(const void* q, const void* k_cache, const void* 
  *    until the process exits.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and keeps it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  A cudaDeviceReset of that device
+ *    later in the process voids the kept address: call this entry point on a
+ *    device only while the context it first ran in is alive.
  *  - Every call uses the same array, which keeps the last call's contents.
  *    Nothing in it has to start at zero: each call writes every partial it
  *    reads.  Calls whose kernels overlap on the GPU (different streams, or

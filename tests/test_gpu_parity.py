@@ -26,6 +26,11 @@ def cpe():
     return lib
 
 
+def _cached(cpe, spec):
+    """The prefix-cache hit of a chunked workload, from the chunk planner."""
+    return cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)[1]
+
+
 def _status_ok(cpe):
     st, detail = cpe.cpe_get_device_status()
     assert st == cpe.CPE_OK, f"device status {cpe.cpe_status_string(st)} detail {detail}"
@@ -118,7 +123,7 @@ def _chunked_run(cpe, spec, device="cuda", one_call=False, n_workspaces=0):
     through cpe_mixed_step with no decode rows (append and schedule share a launch).
     n_workspaces: 0 lets each call allocate its own; 1 reuses one workspace for
     every round; 2 alternates two (the rounds' launches then overlap more)."""
-    req = W.make_chunked(spec, device=device)
+    req = W.make_chunked(spec, _cached(cpe, spec), device=device)
     chunks, _, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
     wss = [cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, device)
            for _ in range(n_workspaces)]
@@ -238,7 +243,7 @@ def test_workspace_rotations_and_two_streams(cpe):
         _, _, out = _chunked_run(cpe, spec, one_call=True, n_workspaces=n)
         assert torch.equal(out, ref), n
     # A,A,B,B,...: every other call reuses the previous call's workspace
-    req = W.make_chunked(spec, device="cuda")
+    req = W.make_chunked(spec, _cached(cpe, spec), device="cuda")
     wss = [cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, "cuda") for _ in range(2)]
     outs = []
     for ch in chunks:
@@ -249,7 +254,7 @@ def test_workspace_rotations_and_two_streams(cpe):
     _status_ok(cpe)
     assert torch.equal(torch.cat(outs), ref)
     # two requests, one per stream, rounds issued alternately from the host
-    reqs = [W.make_chunked(spec, device="cuda") for _ in range(2)]
+    reqs = [W.make_chunked(spec, _cached(cpe, spec), device="cuda") for _ in range(2)]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     wsp = [[cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, "cuda")
             for _ in range(2)] for _ in range(2)]
@@ -288,7 +293,7 @@ def test_prefill_4000_c512_full(cpe):
 
 
 def _sampled_rounds(cpe, spec, round_ids, n_rows, seed):
-    req = W.make_chunked(spec, device="cuda")
+    req = W.make_chunked(spec, _cached(cpe, spec), device="cuda")
     chunks, cached, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
     for ch in chunks:  # every round's keys go into the cache first
         q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
@@ -322,6 +327,43 @@ def test_prefill_128k_c1024_sampled(cpe):
     assert len(chunks) == 128 and chunks[-1].seq_len == 131072
 
 
+def test_prefill_128k_c1024_every_round_as_benchmarked(cpe):
+    """All 128 rounds of prefill-128k-c1024 exactly as the benchmark runs them:
+    one cpe_mixed_step per round (K/V append and extend attention in one
+    call), two workspaces alternated, so every per-round schedule the
+    benchmark times (1 to 5 key-range parts per unit, last-wave fill) is
+    exercised.  In every round the first row, the last row and both rows
+    around one query-tile boundary (a different boundary each round) are
+    compared, all heads and keys, with the float64 oracle."""
+    spec = W.CONFIGS["prefill-128k-c1024"]
+    chunks, cached, _ = cpe.cpe_plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)
+    assert len(chunks) == 128 and cached == 0
+    req = W.make_chunked(spec, cached, device="cuda")
+    wss = [cpe.alloc_workspace(1, spec.chunk, spec.h_q, spec.h_kv, spec.d, spec.input_len, "cuda") for _ in range(2)]
+    out = torch.empty_like(req.q)
+    lse = torch.empty(req.q.shape[0], spec.h_q, dtype=torch.float32, device="cuda")
+    tok = 128 // (spec.h_q // spec.h_kv)  # tokens per query tile
+    rows = []
+    for ch in chunks:
+        a = ch.prefix_len - cached
+        sl = slice(a, a + ch.query_len)
+        cpe.cpe_mixed_step(req.q[sl], req.k[sl], req.v[sl], req.k_cache, req.v_cache, req.page_table,
+                           i32([0, ch.query_len]), i32([ch.prefix_len]), 0, ch.seq_len, out=out[sl], lse=lse[sl],
+                           workspace=wss[ch.index & 1])
+        b = tok * (1 + (ch.index * 37) % (ch.query_len // tok - 1))
+        rows += [a + r for r in (0, b - 1, b, ch.query_len - 1)]
+    _status_ok(cpe)
+    # the whole request as one batch of 128 sequences (one per round) for the oracle
+    qo = [c.prefix_len - cached for c in chunks] + [spec.input_len - cached]
+    pt = torch.tensor([req.page_table_host] * len(chunks), dtype=torch.int32)
+    ref_o, ref_l = oracle.extend_attention(req.q.cpu(), req.k_cache.cpu(), req.v_cache.cpu(), pt, qo,
+                                           [c.prefix_len for c in chunks], spec.h_q, spec.h_kv, rows=rows)
+    for t in range(len(chunks)):
+        r = rows[4 * t:4 * t + 4]
+        check_close(out[r], ref_o[4 * t:4 * t + 4], f"prefill-128k-c1024 round {t} rows {r}")
+        np.testing.assert_allclose(lse[r].cpu().numpy(), ref_l[4 * t:4 * t + 4], atol=LSE_ABS, rtol=0)
+
+
 def test_d64_long_rounds_cut_units_sampled(cpe):
     """d = 64 with rounds long enough that the schedule cuts every unit into
     four or five key-range parts and fills the last wave, so the merge
@@ -331,7 +373,7 @@ def test_d64_long_rounds_cut_units_sampled(cpe):
     chunks = _sampled_rounds(cpe, spec, [0, 7], 32, 700)
     # the last round again, with a workspace whose schedule header can be read:
     # header[7] counts the units cut into parts
-    req = W.make_chunked(spec, device="cuda")
+    req = W.make_chunked(spec, _cached(cpe, spec), device="cuda")
     for ch in chunks:
         q, k, v = req.round_inputs(ch.prefix_len, ch.query_len)
         cpe.cpe_kv_append(k, v, req.k_cache, req.v_cache, req.page_table, i32([0, ch.query_len]),
@@ -432,6 +474,30 @@ def test_mixed_256dec_2048_sampled(cpe):
                                            spec.h_kv, rows=rows)
     check_close(out[256:][rows], ref_o, "mixed-256dec-2048 prefill rows")
     np.testing.assert_allclose(lse[256:][rows].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
+def test_mixed_256dec_2048_every_decode_row(cpe):
+    """The mixed step as the benchmark runs it, all 256 decode rows (all heads,
+    all keys) against the float64 oracle on the whole page pool."""
+    spec = W.CONFIGS["mixed-256dec-2048"]
+    g = torch.Generator().manual_seed(spec.seed)
+    ctx = torch.randint(spec.ctx_lo, spec.ctx_hi + 1, (spec.n_decode,), generator=g).tolist()
+    plan = cpe.cpe_plan_mixed_step(spec.token_budget, ctx, spec.prefill_prefix, spec.prefill_remaining)
+    mb = W.make_mixed(spec, plan["extend_len"], device="cuda")
+    plan = cpe.cpe_plan_mixed_step(spec.token_budget, mb.ctx_len, spec.prefill_prefix, spec.prefill_remaining)
+    nd = plan["n_decode"]
+    assert nd == 256
+    ws = cpe.alloc_workspace(nd + 1, mb.q.shape[0], spec.h_q, spec.h_kv, spec.d, max(plan["kv_len"]), "cuda")
+    lse = torch.empty(mb.q.shape[0], spec.h_q, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(mb.q, mb.k_new, mb.v_new, mb.k_cache, mb.v_cache, mb.page_table,
+                                i32(plan["qo_indptr"]), i32(plan["prefix_len"]), nd, max(plan["kv_len"]), lse=lse,
+                                workspace=ws)
+    _status_ok(cpe)
+    ref_o, ref_l = oracle.extend_attention(mb.q[:nd].cpu(), mb.k_cache.cpu(), mb.v_cache.cpu(),
+                                           mb.page_table_host[:nd], list(range(nd + 1)), plan["prefix_len"][:nd],
+                                           spec.h_q, spec.h_kv)
+    check_close(out[:nd], ref_o, "mixed-256dec-2048 all decode rows")
+    np.testing.assert_allclose(lse[:nd].cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
 
 
 def _scheduled_step(cpe, seed, budget, running, waiting):

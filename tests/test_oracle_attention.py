@@ -136,7 +136,7 @@ def test_chunked_equals_one_shot_fp32_512():
     """The article's exactness claim on the fp32 workload: four 128-token
     extend rounds through the paged cache equal one-shot causal prefill."""
     spec = W.CONFIGS["fp32-512"]
-    req = W.make_chunked(spec)
+    req = W.make_chunked(spec, oracle.plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)[0].prefix_len)
     one, one_lse = oracle.causal_attention(req.q, req.k, req.v, spec.h_q, spec.h_kv)
     outs, lses = [], []
     for ch in oracle.plan_chunks(spec.input_len, spec.hit_rate, spec.chunk):
@@ -153,7 +153,7 @@ def test_chunked_equals_one_shot_fp32_512():
 
 def test_chunked_equals_one_shot_gqa_bf16():
     spec = W.shrink(W.CONFIGS["prefill-4000-c512"], input_len=300, chunk=64, h_q=8, h_kv=2, d=32, page_perm=True)
-    req = W.make_chunked(spec)
+    req = W.make_chunked(spec, oracle.plan_chunks(spec.input_len, spec.hit_rate, spec.chunk)[0].prefix_len)
     one, _ = oracle.causal_attention(req.q, req.k, req.v, spec.h_q, spec.h_kv)
     outs = []
     for ch in oracle.plan_chunks(spec.input_len, 0.0, spec.chunk):
