@@ -348,7 +348,10 @@ cpe_status cpe_decode_attention(const void* q, const void* k_cache, const void* 
  *    returns CPE_ERR_CAPACITY before any launch; split the batch or use
  *    cpe_decode_attention.  Only bf16 is taken (CPE_ERR_UNSUPPORTED).
  *  - The array exists on every GPU that loads the library and stays there
- *    until the process exits.
+ *    until the process exits.  CUDA loads a library's device code lazily by
+ *    default, so the array is placed on a device when the library's first
+ *    kernel there is loaded, which may be this entry point's first call;
+ *    later calls take no device memory.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and keeps it; make that
  *    first call before any stream capture.  A cudaDeviceReset of that device

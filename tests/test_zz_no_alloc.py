@@ -11,8 +11,8 @@ to allocate.
 These tests call that entry point through the C ABI and check it against the
 float64 oracle and against the workspace-based cpe_decode_attention, twice in
 a row (the fixed array is shared by every call and keeps the previous call's
-contents); that a call leaves the device's free memory where it was and
-launches only the decode kernels; and that a batch needing more than the fixed
+contents); that a call after the first leaves the device's free memory where
+it was, and that each call launches only the decode kernels; and that a batch needing more than the fixed
 array is refused before anything is launched.
 """
 import numpy as np
@@ -61,7 +61,7 @@ def test_noalloc_decode_matches_oracle_and_workspace_path_twice():
     # first call: several splits per row; second call: other rows, other sizes
     first = varlen_batch(901, [(L - 1, 1) for L in (1, 17, 2049, 6000, 9000)], 32, 8, 128)
     second = varlen_batch(902, [(L - 1, 1) for L in (4097, 33, 12000)], 16, 4, 64)
-    for b in (first, second):
+    for k, b in enumerate((first, second)):
         out, lse, ref, lse_ref, free0, free1, launched = _both_paths(cpe, b)
         # the float64 oracle on the appended cache (a decode row is an extend row at P = L - 1)
         ref_o, ref_l = oracle.extend_attention(b["q"].cpu(), b["k_cache"].cpu(), b["v_cache"].cpu(),
@@ -70,7 +70,11 @@ def test_noalloc_decode_matches_oracle_and_workspace_path_twice():
         np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
         check_close(out, ref.double().cpu().numpy(), "noalloc vs workspace path", MAX_ABS, REL_RMS)
         np.testing.assert_allclose(lse.cpu().numpy(), lse_ref.cpu().numpy(), atol=LSE_ABS, rtol=0)
-        assert free1 == free0, f"device free memory moved by {free0 - free1} bytes across the call"
+        # The first call in a process may load the library's device module (CUDA
+        # loads modules lazily), which places the fixed array on the device; from
+        # then on a call takes no device memory.
+        if k > 0:
+            assert free1 == free0, f"device free memory moved by {free0 - free1} bytes across the call"
         assert launched in (1, 2), launched  # the decode kernel, and the merge of splits when there are several
 
 
