@@ -7,7 +7,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -114,23 +113,13 @@ bool cached_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows
   return true;
 }
 
-// CTA-pair kernel for head size 128 unless CPE_ONE_CTA=1 (a comparison switch).
-bool pair_path_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("CPE_ONE_CTA");
-    return !(v && v[0] == '1');
-  }();
-  return on;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
   size_t header_off, units_off, items_off, split_off, partial_off, part_o_off, part_ml_off, total;
-  size_t partial_bytes;  // partial-result slots: kMaxSlots two-tile slots' worth at most
-  int unit_capacity, max_splits;
+  int unit_capacity, max_splits, slots;
 };
 
 int group_of(int h_q, int h_kv) { return h_q / h_kv; }
@@ -148,12 +137,11 @@ Layout workspace_layout(int n_seqs, int total_q, int h_q, int h_kv, int d, int m
   L.header_off = 0;
   L.units_off = 256;
   L.items_off = L.units_off + align256(static_cast<size_t>(cap) * sizeof(UnitEntry));
-  const int slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
+  L.slots = static_cast<int>(cap * kMaxParts < kMaxSlots ? cap * kMaxParts : kMaxSlots);
   L.split_off = L.items_off + align256((static_cast<size_t>(cap) * kMaxParts + kMaxCtas) * sizeof(ItemDesc));
-  L.partial_off = L.split_off + align256(static_cast<size_t>(slots / 2 + 1) * sizeof(UnitEntry));
+  L.partial_off = L.split_off + align256(static_cast<size_t>(L.slots / 2 + 1) * sizeof(UnitEntry));
   const size_t parts = static_cast<size_t>(n_seqs) * h_q * L.max_splits;
-  L.partial_bytes = static_cast<size_t>(slots) * partial_slot_bytes(d, kUnitRows);
-  L.part_o_off = L.partial_off + align256(L.partial_bytes);
+  L.part_o_off = L.partial_off + align256(static_cast<size_t>(L.slots) * partial_slot_bytes(d));
   L.part_ml_off = L.part_o_off + align256(parts * d * sizeof(float));
   L.total = L.part_ml_off + align256(parts * 2 * sizeof(float));
   return L;
@@ -295,26 +283,16 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   const ExtendSched sched = sched_of(L, c.workspace);
   const int n_rows = c.total_q - row_begin;
   const int n_seq = c.n_seqs - seq_begin;
-  const int n_sms = persistent_ctas(&e);
-  if (n_sms <= 0) return cuda_fail(fn, e);
-  // head size 128: units of four query tiles on CTA pairs (the two-SM MMA);
-  // head size 64: units of two query tiles, one CTA each
-  const bool pair = c.d == 128 && pair_path_enabled();
-  int workers = n_sms;
-  if (pair) {
-    workers = pair_workers(&e);
-    if (workers <= 0) return cuda_fail(fn, e);
-  }
-  const int unit_tiles = pair ? 4 : 2;
-  const int unit_tok = unit_tiles * tok;
+  // units of two query tiles (256 rows) of one sequence and KV head
+  const int unit_tok = 2 * tok;
   const int cap = c.h_kv * ((n_rows + unit_tok - 1) / unit_tok + n_seq);
-  const int slots = static_cast<int>(L.partial_bytes / partial_slot_bytes(c.d, unit_tiles * kBlockM));
+  const int n_ctas = persistent_ctas(&e);
+  if (n_ctas <= 0) return cuda_fail(fn, e);
 
   ScheduleArgs sa{};
   sa.qo_indptr = c.qo_indptr; sa.prefix_len = c.prefix_len; sa.seq_begin = seq_begin; sa.seq_end = c.n_seqs;
   sa.tok = tok; sa.h_kv = c.h_kv; sa.max_kv_len = c.max_kv_len; sa.max_pages = c.max_pages;
-  sa.capacity = cap; sa.n_ctas = workers; sa.sm_per_cta = pair ? 2 : 1; sa.unit_tiles = unit_tiles;
-  sa.max_slots = slots; sa.cut_slots = slots / 2; sa.sched = sched; sa.status = status;
+  sa.capacity = cap; sa.n_ctas = n_ctas; sa.max_slots = L.slots; sa.sched = sched; sa.status = status;
   sa.d = c.d;
   sa.dec_rows = dec_rows;
   sa.sched_wait = reuses_workspace(stream, c.workspace) ? 1 : 0;
@@ -332,23 +310,20 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
       !cached_map(&a.tm_k, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
       !cached_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
       !cached_map(&a.tm_k128, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
-      !cached_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
-      (pair && !cached_map(&a.tm_k64, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, 64)))
+      !cached_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN))
     return fail(CPE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
   a.page_table = c.page_table; a.qo_indptr = c.qo_indptr; a.prefix_len = c.prefix_len; a.sched = sched;
   a.out = c.out; a.lse = c.lse; a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages;
   a.h_q = c.h_q; a.h_kv = c.h_kv; a.group = G; a.tok = tok; a.d = c.d;
   a.scale_log2 = c.sm_scale * 1.4426950408889634f;
   a.wait_ns = static_cast<uint64_t>(g_wait_ns.load() < 0 ? 0 : g_wait_ns.load());
-  a.n_ctas = workers;
-  a.unit_tiles = unit_tiles;
-  a.sms = n_sms;
-  a.max_split = std::max(1, std::min(cap, slots / 2));  // cut units: at most one per unit, two slots each
+  a.n_ctas = n_ctas;
+  a.max_split = std::max(1, std::min(cap, L.slots / 2));  // cut units: at most one per unit, two slots each
   if (dec_rows > 0) {
     a.dec = decode_args(c, L, dec_rows, true, status);
     a.dec_items = dec_rows * c.h_kv * L.max_splits;
   }
-  e = pair ? launch_extend_pair(a, stream, dependent) : launch_extend_tc(a, stream, dependent);
+  e = launch_extend_tc(a, stream, dependent);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 2;  // the extend kernel and the merge of key-range parts
   if (dec_rows > 0 && L.max_splits > 1) {

@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       if (it.kv_lo >= jhi) {
         // no key tile of this portion reaches this query tile: an empty partial
         if (!it.whole) {  // l = 0 tells the merge to skip this part's O
-          float* ml = reinterpret_cast<float*>(a.sched.partial + static_cast<size_t>(it.slot) * partial_slot_bytes(D, kUnitRows) +
+          float* ml = reinterpret_cast<float*>(a.sched.partial + static_cast<size_t>(it.slot) * partial_slot_bytes(D) +
                                                static_cast<size_t>(kUnitRows) * D * 2);
           ml[R] = -INFINITY;
           ml[kUnitRows + R] = 0.f;
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           a.lse[static_cast<int64_t>(it.q0 + i) * a.h_q + head] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       } else {
         // one part of a unit: the normalised partial goes to the item's slot
-        uint8_t* slot = a.sched.partial + static_cast<size_t>(it.slot) * partial_slot_bytes(D, kUnitRows);
+        uint8_t* slot = a.sched.partial + static_cast<size_t>(it.slot) * partial_slot_bytes(D);
         uint4* prow = reinterpret_cast<uint4*>(slot + static_cast<size_t>(R) * D * 2);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -625,10 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 // Work item w of extend_merge_kernel (see there).
 template <int D>
 __device__ __forceinline__ void merge_rows(const ExtendTcArgs& a, int w) {
-  const int groups = 4 * a.unit_tiles;          // 32-row work items per unit
-  const int unit_rows = a.unit_tiles * kBlockM;
-  const size_t slot_bytes = partial_slot_bytes(D, unit_rows);
-  const UnitEntry e = a.sched.split[w / groups];
+  const UnitEntry e = a.sched.split[w / kMergeRowGroups];
   const int len = (e.n_kv + e.parts - 1) / e.parts;
   const int live = (e.n_kv + len - 1) / len;  // parts that hold key tiles
   const int q0 = a.qo_indptr[e.seq];
@@ -636,8 +633,8 @@ __device__ __forceinline__ void merge_rows(const ExtendTcArgs& a, int w) {
   constexpr int kW = D / 64;  // 32-bit words (bf16 pairs) per lane and row
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int row0 = (w % groups) * 32 + warp * 4;
-  const uint8_t* slot0 = a.sched.partial + static_cast<size_t>(e.slot) * slot_bytes;
+  const int row0 = (w % kMergeRowGroups) * 32 + warp * 4;
+  const uint8_t* slot0 = a.sched.partial + static_cast<size_t>(e.slot) * partial_slot_bytes(D);
 #pragma unroll 1
   for (int rr = 0; rr < 4; rr += 2) {
     float m[2][kMaxParts], l[2][kMaxParts];
@@ -648,10 +645,10 @@ __device__ __forceinline__ void merge_rows(const ExtendTcArgs& a, int w) {
 #pragma unroll
       for (int p = 0; p < kMaxParts; ++p) {
         if (p < live) {
-          const uint8_t* slot = slot0 + static_cast<size_t>(p) * slot_bytes;
-          const float* ml = reinterpret_cast<const float*>(slot + static_cast<size_t>(unit_rows) * D * 2);
+          const uint8_t* slot = slot0 + static_cast<size_t>(p) * partial_slot_bytes(D);
+          const float* ml = reinterpret_cast<const float*>(slot + static_cast<size_t>(kUnitRows) * D * 2);
           m[h][p] = ml[R];
-          l[h][p] = ml[unit_rows + R];
+          l[h][p] = ml[kUnitRows + R];
           const uint32_t* row = reinterpret_cast<const uint32_t*>(slot + static_cast<size_t>(R) * D * 2) + lane * kW;
           if constexpr (kW == 2) {
             const uint2 x = *reinterpret_cast<const uint2*>(row);
@@ -673,7 +670,7 @@ __device__ __forceinline__ void merge_rows(const ExtendTcArgs& a, int w) {
       const int R = row0 + rr + h;
       const int t = R / kBlockM;
       const int r = R % kBlockM;
-      const int i = (a.unit_tiles * e.pair + t) * a.tok + r / a.group;
+      const int i = (2 * e.pair + t) * a.tok + r / a.group;
       if (i >= E) continue;
       float M = -INFINITY;
 #pragma unroll
@@ -713,8 +710,8 @@ __device__ __forceinline__ void merge_rows(const ExtendTcArgs& a, int w) {
 // 2^(m_p - M) * l_p of the normalised part outputs) and write its rows.  The
 // grid is persistent (two blocks per SM, all resident, so the next launch is
 // released at once); block b takes work items b, b + gridDim.x, ..., item
-// w being rows [32 g, 32 g + 32), g = w mod (4 U), of the (w / (4 U))-th cut
-// unit (U query tiles of 128 rows per unit).  Each of the 8 warps takes four of the
+// w being rows [32 g, 32 g + 32), g = w mod kMergeRowGroups, of the
+// (w / kMergeRowGroups)-th cut unit.  Each of the 8 warps takes four of the
 // rows, two at a time, with every part's loads in flight at once; lane l holds
 // columns [l D / 32, (l + 1) D / 32), so one part of one row is one coalesced
 // read.
@@ -724,7 +721,7 @@ __global__ void __launch_bounds__(kMergeThreads) extend_merge_kernel(const __gri
   // depend on this one (its own reads of the cache wait for this launch).
   grid_launch_dependents();
   grid_dependency_wait();  // the extend launch's partials are complete
-  const int n_work = a.sched.header[7] * 4 * a.unit_tiles;
+  const int n_work = a.sched.header[7] * kMergeRowGroups;
   for (int w = blockIdx.x; w < n_work; w += gridDim.x) merge_rows<D>(a, w);
 }
 
@@ -853,7 +850,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
   int carry = 0;
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     const int k = c0 + tid;
-    const int np = k < n ? (seq_tiles(a, a.seq_begin + k, true) + a.unit_tiles - 1) / a.unit_tiles : 0;
+    const int np = k < n ? (seq_tiles(a, a.seq_begin + k, true) + 1) / 2 : 0;
     int chunk_total = 0;
     const int off = carry + block_exclusive_scan(np, &chunk_total, warp_sums);
     if (k < n) seq_off[k] = off;
@@ -890,7 +887,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
     unit_of(u, s, pair, g);
     const int E = a.qo_indptr[s + 1] - a.qo_indptr[s];
     const int P = a.prefix_len[s];
-    const int i_last = min(E, (pair + 1) * a.unit_tiles * a.tok);  // tokens [0, i_last) of the unit's rows
+    const int i_last = min(E, (2 * pair + 2) * a.tok);  // tokens [0, i_last) of the unit's rows
     const int n_kv = (P + i_last + kBlockN - 1) / kBlockN;
     if (unit_cached)
       s_nkv[u] = n_kv;  // the unit entry is written once its parts are known
@@ -940,13 +937,9 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
       const float t_tile = kTileUsPerSm * kFusedExtendSlowdown * static_cast<float>(a.d) / 128.f;
       int best_n = max(1, a.n_ctas - 1);
       float best_t = 3.4e38f;
-      // (a worker is one CTA or a CTA pair; a key tile of a pair's unit
-      // takes a pair about what one of a CTA's unit takes a CTA)
-      const int step = 4 / a.sm_per_cta;
-      for (int nx = step; nx <= a.n_ctas - step; nx += step) {
+      for (int nx = 4; nx <= a.n_ctas - 4; nx += 4) {
         const float te = static_cast<float>(W) * t_tile / nx;
-        const float td =
-            t_dec * fmaxf(1.f, static_cast<float>(kDecodeSatSms) / ((a.n_ctas - nx) * a.sm_per_cta));
+        const float td = t_dec * fmaxf(1.f, static_cast<float>(kDecodeSatSms) / (a.n_ctas - nx));
         if (fmaxf(te, td) < best_t) {
           best_t = fmaxf(te, td);
           best_n = nx;
@@ -980,7 +973,7 @@ __device__ __forceinline__ void schedule_body(const ScheduleArgs& a) {
       const int T = max(1, (n_max + S - 1) / S);
       const int items = sums16[S - 1];
       const int slots = S > 1 ? sums16[kMaxParts + S - 1] : 0;
-      if (slots > min(a.max_slots, a.cut_slots)) break;
+      if (slots > min(a.max_slots, kCutSlots)) break;
       const int ncp = max(1, min(n_ext, items));
       const int waves = (items + ncp - 1) / ncp;
       const float t = waves * (T + kItemCostTiles) + (S > 1 ? kMergeCostTiles : 0.f);
@@ -1227,19 +1220,18 @@ cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool depende
   if (a.n_ctas <= 0) return cudaSuccess;
   cudaError_t e = a.d == 128 ? prepare_extend<128>() : prepare_extend<64>();
   if (e != cudaSuccess) return e;
-  if (a.d == 128)
-    e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, TcCfg<128>::kSmem, s, a, dependent);
-  else
-    e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, TcCfg<64>::kSmem, s, a, dependent);
-  if (e != cudaSuccess) return e;
-  return launch_extend_merge(a, s, dependent);
-}
-
-cudaError_t launch_extend_merge(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
   // the merge's persistent grid: two blocks per SM, fewer if there cannot be that much work
-  const int merge_grid = std::max(1, std::min(a.max_split * 4 * a.unit_tiles, 2 * a.sms));
-  if (a.d == 128) return launch_dependent(extend_merge_kernel<128>, merge_grid, kMergeThreads, 0, s, a, dependent);
-  return launch_dependent(extend_merge_kernel<64>, merge_grid, kMergeThreads, 0, s, a, dependent);
+  const int merge_grid = std::max(1, std::min(a.max_split * kMergeRowGroups, 2 * a.n_ctas));
+  if (a.d == 128) {
+    e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, TcCfg<128>::kSmem, s, a, dependent);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(extend_merge_kernel<128>, merge_grid, kMergeThreads, 0, s, a, dependent);
+  } else {
+    e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, TcCfg<64>::kSmem, s, a, dependent);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(extend_merge_kernel<64>, merge_grid, kMergeThreads, 0, s, a, dependent);
+  }
+  return e;
 }
 
 }  // namespace cpe

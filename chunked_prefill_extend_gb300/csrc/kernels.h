@@ -24,14 +24,15 @@ constexpr float kItemCostTiles = 3.0f;
 constexpr float kMergeCostTiles = 4.0f;
 constexpr int kSizeBuckets = 4;      // item-size classes of the largest-first order
 constexpr int kPairBits = 20;        // ItemDesc::head_pair = kv_head << kPairBits | pair
-constexpr int kMaxSlots = 2048;      // partial-result slots of two-tile units in the workspace
-constexpr int kUnitRows = 2 * kBlockM;      // rows of a one-CTA unit: two query tiles
-constexpr int kPairUnitRows = 4 * kBlockM;  // rows of a CTA-pair unit: four query tiles
-constexpr int kMergeThreads = 256;  // merge block: 8 warps, four rows each; a work item is 32 rows
+constexpr int kMaxSlots = 2048;      // partial-result slots in the workspace
+constexpr int kCutSlots = 1024;      // of which the uniform cut may use (the rest fill the last wave)
+constexpr int kUnitRows = 2 * kBlockM;
+constexpr int kMergeRowGroups = 8;  // merge work items per cut unit (32 rows each)
+constexpr int kMergeThreads = 256;  // merge block: 8 warps, four rows each
 
-struct UnitEntry {  // one extend work unit: U query tiles (U = 2, or 4 on a CTA pair) of one sequence and KV head
+struct UnitEntry {  // one extend work unit: two query tiles of one sequence and KV head
   int seq;
-  int pair;      // unit index in the sequence: query tiles [U*pair, U*pair + U)
+  int pair;      // query tiles 2*pair and 2*pair+1 of the sequence
   int kv_head;
   int n_kv;      // key tiles the unit needs
   int parts;     // key-range parts the unit is cut into (1: it writes its output directly)
@@ -62,13 +63,13 @@ struct ExtendSched {
                         // decode item of a fused mixed step, [7] units cut into parts
   UnitEntry* units;     // [capacity]
   ItemDesc* items;      // [item capacity]
-  uint8_t* partial;     // slots of partial_slot_bytes(d, rows): O [rows x d] bf16 (normalised), then
-                        // m [rows] (log2) and l [rows] fp32, rows = the unit's rows
+  uint8_t* partial;     // slots of partial_slot_bytes(d): O [256 x d] bf16 (normalised), then m [256]
+                        // (log2) and l [256] fp32
   UnitEntry* split;     // the units cut into parts, in unit order (header[7] of them)
 };
 
-__host__ __device__ constexpr size_t partial_slot_bytes(int d, int unit_rows) {
-  return size_t(unit_rows) * d * 2 + 2 * size_t(unit_rows) * 4;
+__host__ __device__ constexpr size_t partial_slot_bytes(int d) {
+  return size_t(kUnitRows) * d * 2 + 2 * size_t(kUnitRows) * 4;
 }
 
 struct DecodeArgs {
@@ -110,11 +111,8 @@ struct ScheduleArgs {
   int max_kv_len;
   int max_pages;
   int capacity;             // unit entries available
-  int n_ctas;               // persistent workers: CTAs, or CTA pairs
-  int sm_per_cta;           // SMs one worker occupies (1, or 2 for a CTA pair)
-  int unit_tiles;           // query tiles per unit (2, or 4 on a CTA pair)
+  int n_ctas;               // persistent grid size
   int max_slots;            // partial slots available
-  int cut_slots;            // of which the uniform cut may use (the rest fill the last wave)
   ExtendSched sched;
   int* status;
   // fused mixed step: decode rows [0, dec_rows) run on the CTAs the extend
@@ -131,7 +129,6 @@ struct ScheduleArgs {
 struct ExtendTcArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   CUtensorMap tm_k128, tm_v128;  // the same caches with 128-token boxes (8 consecutive pages)
-  CUtensorMap tm_k64;            // the K cache with 64-token boxes (4 consecutive pages; CTA pairs)
   const int32_t* page_table;
   const int32_t* qo_indptr;
   const int32_t* prefix_len;
@@ -144,10 +141,8 @@ struct ExtendTcArgs {
   int h_q, h_kv, group, tok, d;
   float scale_log2;
   uint64_t wait_ns;
-  int n_ctas;      // persistent workers: CTAs, or CTA pairs (the grid is then 2 n_ctas)
-  int unit_tiles;  // query tiles per unit (2, or 4 on a CTA pair)
-  int max_split;   // units that may be cut into parts (bounds the merge kernel's grid)
-  int sms;         // SMs of the device (the merge kernel's grid is two blocks per SM at most)
+  int n_ctas;
+  int max_split;  // units that may be cut into parts (the merge kernel's grid / kMergeRowGroups)
   // fused mixed step: CTAs past the extend part run these decode items
   // ((sequence x KV head) x split, split fastest), taken from header[6]
   DecodeArgs dec;
@@ -195,13 +190,6 @@ cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream
 // ones (measured on the 128k-token request's 1.7 ms rounds) it costs about 1 %, so the caller
 // turns it on only below kDependentLaunchFlops of extend work.
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent);
-// The same on CTA pairs (d = 128): extend_pair_kernel + the merge.  a.n_ctas
-// counts pairs (at most pair_workers()).
-cudaError_t launch_extend_pair(const ExtendTcArgs& a, cudaStream_t s, bool dependent);
-// CTA pairs the pair kernel may keep resident on the current device (0 on error).
-int pair_workers(cudaError_t* err);
-// The merge of key-range parts alone (after either extend kernel).
-cudaError_t launch_extend_merge(const ExtendTcArgs& a, cudaStream_t s, bool dependent);
 constexpr double kDependentLaunchFlops = 2e11;
 cudaError_t launch_extend_simt(const ExtendSimtArgs& a, cudaStream_t s);
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t s);
