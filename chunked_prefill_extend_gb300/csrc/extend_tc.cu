@@ -90,11 +90,17 @@ struct TcCfg {
   static constexpr int kSmem = kBarOff + 512 + 1024;  // + barriers + alignment slack
 };
 
+// Ring slots are released per key tile: one commit after a key tile's MMAs
+// arrives on rel[r % NR] (r counts key tiles over the CTA's items) and frees
+// V_r and every K tile whose S products were issued by then.  NR exceeds both
+// ring depths, so a producer waiting on a release cannot miss its phase.
 template <int NK, int NV>
 struct Bars {
+  static constexpr int NR = (NK > NV ? NK : NV) + 1;
   uint64_t q_full, q_empty;
-  uint64_t k_full[NK], k_empty[NK];
-  uint64_t v_full[NV], v_empty[NV];
+  uint64_t k_full[NK];
+  uint64_t v_full[NV];
+  uint64_t rel[NR];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -208,14 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int i = 0; i < NK; ++i) {
-      mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->k_empty[i], 1);
-    }
-    for (int i = 0; i < NV; ++i) {
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->v_empty[i], 1);
-    }
+    for (int i = 0; i < NK; ++i) mbar_init(&bars->k_full[i], 1);
+    for (int i = 0; i < NV; ++i) mbar_init(&bars->v_full[i], 1);
+    for (int i = 0; i < Bars<NK, NV>::NR; ++i) mbar_init(&bars->rel[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4);
@@ -238,14 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const CUtensorMap* tm128 = is_k ? &a.tm_k128 : &a.tm_v128;
       const int ns = is_k ? NK : NV;
       uint64_t* full = is_k ? bars->k_full : bars->v_full;
-      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
       prefetch_tmap(tm);
       prefetch_tmap(tm128);
       if (is_k) prefetch_tmap(&a.tm_q);
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
-      int cnt = 0;       // ring loads issued so far
+      constexpr int NR = Bars<NK, NV>::NR;
+      int cnt = 0;       // ring loads issued so far (= key tiles, over the CTA's items)
       int items = 0;     // Q loads issued so far
+      uint32_t firsts = 0;  // bit i: load cnt - 1 - i was the first key tile of its item
       bool ok = true;
       Item it;
       for (int wi = cta; ok && wi < n_items; wi += nc) {
@@ -283,11 +285,19 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
               contiguous = contiguous && rows[pg] == rows[0] + pg * kPage;
             }
           }
-          if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, abort, a.wait_ns, a.status,
-                                    is_k ? kDetailKEmpty : kDetailVEmpty)) {
-            ok = false;
-            break;
+          // The load this one replaces, m = cnt - ns, was released with key
+          // tile m's MMAs; a K tile whose S products were issued one key tile
+          // earlier (every K tile but an item's first) already with key tile m - 1.
+          if (use > 0) {
+            const int m = cnt - ns;
+            const int r = (is_k && !((firsts >> (ns - 1)) & 1u)) ? m - 1 : m;
+            if (!mbar_wait(&bars->rel[r % NR], (r / NR) & 1, abort, a.wait_ns, a.status,
+                           is_k ? kDetailKEmpty : kDetailVEmpty)) {
+              ok = false;
+              break;
+            }
           }
+          firsts = (firsts << 1) | (j == it.kv_lo ? 1u : 0u);
           mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
           if (contiguous) {
             for (int h = 0; h < C::kHalves; ++h)
@@ -325,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_commit(&bars->s_full[t]);
       };
       int kc = 0, vc = 0, items = 0;
+      int rs = 0;  // release barrier of the next key tile
       int pc0 = 0, pc1 = 0;  // P hand-offs consumed per tile
       bool ok = true;
       Item it;
@@ -339,7 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_fence_after();
         if (it.kv_lo < it.n_kt_0) issue_s(0, kc % NK);
         if (it.kv_lo < it.n_kt_1) issue_s(1, kc % NK);
-        tc_commit(&bars->k_empty[kc % NK]);
         ++kc;
         for (int j = it.kv_lo; j < it.kv_hi; ++j) {
           // Both operand stages this key tile needs are waited for up front, so
@@ -397,12 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             ok = false;
             break;
           }
-          tc_commit(&bars->v_empty[sv_st]);
+          // one release per key tile: V_j, and K_{j+1} (and K_j at an item's start)
+          tc_commit(&bars->rel[rs]);
+          rs = rs + 1 == Bars<NK, NV>::NR ? 0 : rs + 1;
           ++vc;
-          if (more) {
-            tc_commit(&bars->k_empty[kc % NK]);
-            ++kc;
-          }
+          if (more) ++kc;
         }
         tc_commit(&bars->q_empty);  // every S of this item issued: Q may be replaced
       }
