@@ -91,7 +91,7 @@ bool cached_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows
     int64_t rows;
     int d, heads, box_heads, box_rows;
   };
-  constexpr int kEntries = 8;
+  constexpr int kEntries = 16;
   thread_local Entry cache[kEntries] = {};
   thread_local int next = 0;
   for (const Entry& e : cache)
@@ -300,7 +300,18 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   // dependent launches hide launch latency; worth it only on short launches
   const double flops_bound = 4.0 * c.d * c.h_q * static_cast<double>(n_rows) * c.max_kv_len;
   const bool dependent = flops_bound < kDependentLaunchFlops;
-  e = append ? launch_prep(sa, *append, stream, dependent) : launch_schedule(sa, stream, dependent);
+  // With the round's new rows at hand, a long extend launch reads the chunk's
+  // keys from them and writes the full new pages of page-aligned sequences
+  // into the cache itself; the prep launch appends the rest.  (On short
+  // launches the stores' share of the time measured a few percent slower than
+  // the prep launch's append, so there the prep launch appends every row.)
+  const bool staged = append != nullptr && !dependent;
+  KvAppendArgs ka{};
+  if (append) {
+    ka = *append;
+    ka.staged_from = staged ? seq_begin : c.n_seqs;
+  }
+  e = append ? launch_prep(sa, ka, stream, dependent) : launch_schedule(sa, stream, dependent);
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 1;
 
@@ -310,11 +321,16 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
       !cached_map(&a.tm_k, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
       !cached_map(&a.tm_v, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kPage) ||
       !cached_map(&a.tm_k128, c.k_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
-      !cached_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN))
+      !cached_map(&a.tm_v128, c.v_cache, c.d, c.h_kv, c.num_pages * kPage, 1, kBlockN) ||
+      (staged && (!cached_map(&a.tm_kn, append->k_new, c.d, c.h_kv, c.total_q, 1, kPage) ||
+                  !cached_map(&a.tm_vn, append->v_new, c.d, c.h_kv, c.total_q, 1, kPage) ||
+                  !cached_map(&a.tm_kn128, append->k_new, c.d, c.h_kv, c.total_q, 1, kBlockN) ||
+                  !cached_map(&a.tm_vn128, append->v_new, c.d, c.h_kv, c.total_q, 1, kBlockN))))
     return fail(CPE_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed");
   a.page_table = c.page_table; a.qo_indptr = c.qo_indptr; a.prefix_len = c.prefix_len; a.sched = sched;
   a.out = c.out; a.lse = c.lse; a.status = status; a.num_pages = c.num_pages; a.max_pages = c.max_pages;
   a.h_q = c.h_q; a.h_kv = c.h_kv; a.group = G; a.tok = tok; a.d = c.d;
+  a.staged = staged ? 1 : 0;
   a.scale_log2 = c.sm_scale * 1.4426950408889634f;
   a.wait_ns = static_cast<uint64_t>(g_wait_ns.load() < 0 ? 0 : g_wait_ns.load());
   a.n_ctas = n_ctas;
@@ -406,6 +422,7 @@ cpe_status cpe_kv_append(const void* k_new, const void* v_new, void* k_cache, vo
   a.qo_indptr = qo_indptr; a.prefix_len = prefix_len; a.status = status; a.num_pages = num_pages;
   a.max_pages = max_pages; a.n_seqs = n_seqs; a.total_q = total_q; a.row_bytes = static_cast<int>(row_bytes);
   a.page_size = page_size;
+  a.staged_from = n_seqs;  // every row
   e = launch_kv_append(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(fn, e);
   g_launches += 1;

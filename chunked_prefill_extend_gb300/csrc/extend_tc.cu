@@ -101,6 +101,9 @@ struct Bars {
   uint64_t k_full[NK];
   uint64_t v_full[NV];
   uint64_t rel[NR];
+  // cache-page stores owed from each slot's current tile (kept by the slot's
+  // producer): pages mask, sequence, key tile, KV head
+  int k_owed[NK][4], v_owed[NV][4];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -152,6 +155,23 @@ __device__ __forceinline__ bool load_item(const ExtendTcArgs& a, int i, Item& it
   return true;
 }
 
+// Pages of key tile j (keys kb + 16 pg) that an item of a page-aligned
+// sequence writes to the cache from its staged tile: new pages (keys >= P,
+// pg >= pnew) that are full pages of the unit's own tokens
+// [P + i0_0, P + min(E, i0_0 + 2 tok)).  Each full new page of a sequence and
+// KV head belongs to exactly one unit, and its key tile to one part.
+__device__ __forceinline__ uint32_t own_pages(const Item& it, int tok, int kb, int pnew, int npg) {
+  const int own_lo = it.P + it.i0_0;
+  const int own_hi = it.P + min(it.E, it.i0_0 + 2 * tok);
+  uint32_t m = 0;
+#pragma unroll
+  for (int pg = 0; pg < kBlockN / kPage; ++pg) {
+    const int pos = kb + pg * kPage;
+    if (pg >= pnew && pg < npg && pos >= own_lo && pos + kPage <= own_hi) m |= 1u << pg;
+  }
+  return m;
+}
+
 // Decode rows of a fused mixed step on a CTA the extend part does not use:
 // each of the CTA's three warpgroups takes decode items from the shared
 // counter and computes them as the stand-alone decode kernel's CTAs do, in its
@@ -184,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars<NK, NV>* bars = reinterpret_cast<Bars<NK, NV>*>(smem + C::kBarOff);
+  static_assert(sizeof(Bars<NK, NV>) <= 512, "barrier area");
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -217,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     for (int i = 0; i < NK; ++i) mbar_init(&bars->k_full[i], 1);
     for (int i = 0; i < NV; ++i) mbar_init(&bars->v_full[i], 1);
     for (int i = 0; i < Bars<NK, NV>::NR; ++i) mbar_init(&bars->rel[i], 1);
+    for (int i = 0; i < NK; ++i) bars->k_owed[i][0] = 0;
+    for (int i = 0; i < NV; ++i) bars->v_owed[i][0] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4);
@@ -237,17 +260,43 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const bool is_k = warp == 0;
       const CUtensorMap* tm = is_k ? &a.tm_k : &a.tm_v;
       const CUtensorMap* tm128 = is_k ? &a.tm_k128 : &a.tm_v128;
+      const CUtensorMap* tmn = is_k ? &a.tm_kn : &a.tm_vn;        // the round's new rows
+      const CUtensorMap* tmn128 = is_k ? &a.tm_kn128 : &a.tm_vn128;
       const int ns = is_k ? NK : NV;
       uint64_t* full = is_k ? bars->k_full : bars->v_full;
       uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
       prefetch_tmap(tm);
       prefetch_tmap(tm128);
+      if (a.staged) {
+        prefetch_tmap(tmn);
+        prefetch_tmap(tmn128);
+      }
       if (is_k) prefetch_tmap(&a.tm_q);
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
       constexpr int NR = Bars<NK, NV>::NR;
       int cnt = 0;       // ring loads issued so far (= key tiles, over the CTA's items)
       int items = 0;     // Q loads issued so far
       uint32_t firsts = 0;  // bit i: load cnt - 1 - i was the first key tile of its item
+      int (*owed)[4] = is_k ? bars->k_owed : bars->v_owed;
+      // The full new pages of a page-aligned sequence's own tokens are written
+      // to the cache from the slot they were staged in, when the slot is
+      // refilled (its tile has landed and been consumed by then) or, for the
+      // last tiles, once they land at the end.
+      auto store_owed = [&](int st) {
+        const int* o = owed[st];
+        const int32_t* opt = a.page_table + static_cast<int64_t>(o[1]) * a.max_pages;
+#pragma unroll
+        for (int pg = 0; pg < kBlockN / kPage; ++pg) {
+          if (!((o[0] >> pg) & 1)) continue;
+          const int pid = opt[o[2] * (kBlockN / kPage) + pg];
+          if (pid < 0 || pid >= a.num_pages) continue;  // recorded when the tile was loaded
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_store_3d(tm, ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), h * 64, o[3],
+                         pid * kPage);
+        }
+        bulk_commit_group();
+        owed[st][0] = 0;
+      };
       bool ok = true;
       Item it;
       for (int wi = cta; ok && wi < n_items; wi += nc) {
@@ -265,13 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
         const int kv_max = max(it.kv_end_0, it.kv_end_1);
         const int32_t* pt = a.page_table + static_cast<int64_t>(it.seq) * a.max_pages;
+        // A prefix that ends on a page boundary: the chunk's keys are read from
+        // the round's new rows, and the full pages of this unit's own tokens
+        // (keys P + [2 pair tok, 2 pair tok + 2 tok)) are written to the cache
+        // from the staged tile.  Otherwise everything comes from the cache.
+        const bool staged = a.staged && it.P % kPage == 0;
         for (int j = it.kv_lo; j < it.kv_hi; ++j, ++cnt) {
           const int st = cnt % ns;
           const int use = cnt / ns;
-          const int keys = min(kBlockN, kv_max - j * kBlockN);
+          const int kb = j * kBlockN;
+          const int keys = min(kBlockN, kv_max - kb);
           const int npg = (keys + kPage - 1) / kPage;
+          const int pnew = staged ? min(npg, max(0, (it.P - kb) / kPage)) : npg;  // pages [pnew, npg) are new
           int rows[kBlockN / kPage];  // unrolled loops below keep it in registers
-          bool contiguous = npg == kBlockN / kPage;  // eight pages back to back: one box per half
+          bool contiguous = npg == kBlockN / kPage && pnew == npg;  // eight cached pages back to back
 #pragma unroll
           for (int pg = 0; pg < kBlockN / kPage; ++pg) {
             if (pg >= npg) break;
@@ -297,18 +353,36 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
               break;
             }
           }
+          if (a.staged && owed[st][0]) {  // the slot's previous tile owes cache pages: store them, let them read the slot
+            store_owed(st);
+            bulk_wait_read_all();
+          }
+          if (staged) {
+            const uint32_t own = own_pages(it, a.tok, kb, pnew, npg);
+            if (own) {
+              owed[st][0] = static_cast<int>(own);
+              owed[st][1] = it.seq;
+              owed[st][2] = j;
+              owed[st][3] = it.g;
+            }
+          }
           firsts = (firsts << 1) | (j == it.kv_lo ? 1u : 0u);
+          uint8_t* dst = ring + st * C::kTileBytes;
           mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
           if (contiguous) {
             for (int h = 0; h < C::kHalves; ++h)
-              tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes, tm128, &full[st], h * 64, it.g, rows[0]);
+              tma_load_3d(dst + h * C::kHalfBytes, tm128, &full[st], h * 64, it.g, rows[0]);
+          } else if (pnew == 0 && npg == kBlockN / kPage) {  // eight new pages: rows q0 + kb - P onwards
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(dst + h * C::kHalfBytes, tmn128, &full[st], h * 64, it.g, it.q0 + kb - it.P);
           } else {
 #pragma unroll
             for (int pg = 0; pg < kBlockN / kPage; ++pg) {
               if (pg >= npg) break;
+              const bool nw = pg >= pnew;
               for (int h = 0; h < C::kHalves; ++h)
-                tma_load_3d(ring + st * C::kTileBytes + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64,
-                            it.g, rows[pg]);
+                tma_load_3d(dst + h * C::kHalfBytes + pg * (kPage * 128), nw ? tmn : tm, &full[st], h * 64, it.g,
+                            nw ? it.q0 + kb + pg * kPage - it.P : rows[pg]);
             }
           }
         }
@@ -319,7 +393,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (is_k && items > 0) mbar_wait(&bars->q_full, (items - 1) & 1, no_abort, kDrainNs, a.status, kDetailDrain);
         for (int n = max(0, cnt - ns); n < cnt; ++n)
           mbar_wait(&full[n % ns], (n / ns) & 1, no_abort, kDrainNs, a.status, kDetailDrain);
+      } else if (a.staged) {
+        // the last tiles' owed pages, once each has landed
+        for (int n = max(0, cnt - ns); n < cnt; ++n) {
+          if (!owed[n % ns][0]) continue;
+          if (!mbar_wait(&full[n % ns], (n / ns) & 1, abort, a.wait_ns, a.status, is_k ? kDetailKFull : kDetailVFull))
+            break;
+          store_owed(n % ns);
+        }
       }
+      if (a.staged) bulk_wait_read_all();  // no store still reads the ring when the CTA leaves
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);

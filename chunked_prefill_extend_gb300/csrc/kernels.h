@@ -129,6 +129,12 @@ struct ScheduleArgs {
 struct ExtendTcArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   CUtensorMap tm_k128, tm_v128;  // the same caches with 128-token boxes (8 consecutive pages)
+  // the round's new K/V rows [total_q, h_kv, d] (16- and 128-row boxes), when
+  // the call has them (staged = 1): for a sequence whose prefix ends on a page
+  // boundary the extend launch reads its new keys from these rows and writes
+  // the full new pages into the cache from the tiles it staged
+  CUtensorMap tm_kn, tm_vn, tm_kn128, tm_vn128;
+  int staged;
   const int32_t* page_table;
   const int32_t* qo_indptr;
   const int32_t* prefix_len;
@@ -176,6 +182,10 @@ struct KvAppendArgs {
   int* status;
   int64_t num_pages;
   int max_pages, n_seqs, total_q, row_bytes, page_size;
+  // sequences >= staged_from whose prefix ends on a page boundary have their
+  // full new pages written by the extend launch: their rows there are skipped
+  // (n_seqs: append every row)
+  int staged_from;
 };
 
 

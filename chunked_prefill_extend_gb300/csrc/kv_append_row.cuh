@@ -28,6 +28,11 @@ __device__ __forceinline__ void append_row(const KvAppendArgs& a, int row, int l
   if (row >= a.total_q) return;
   const int s = seq_of_row(a.qo_indptr, a.n_seqs, row);
   const int pos = a.prefix_len[s] + row - a.qo_indptr[s];
+  if (s >= a.staged_from && a.prefix_len[s] % a.page_size == 0) {
+    // the extend launch writes this sequence's full new pages from its staged tiles
+    const int full = (a.qo_indptr[s + 1] - a.qo_indptr[s]) / a.page_size * a.page_size;
+    if (row - a.qo_indptr[s] < full) return;
+  }
   const int pidx = pos / a.page_size;
   if (pos < 0 || pidx >= a.max_pages) {
     if (lane == 0) record_error(a.status, kStatusDeviceArg, kDetailBadLength);

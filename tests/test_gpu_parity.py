@@ -64,6 +64,34 @@ def test_kv_append_bitwise(cpe, dtype):
     assert torch.equal(b["k_cache"].cpu(), kc_ref) and torch.equal(b["v_cache"].cpu(), vc_ref)
 
 
+@pytest.mark.parametrize("h_q,h_kv,d,n_decode,long_seq", [(32, 8, 128, 0, None), (32, 8, 128, 0, (8192, 1024)),
+                                                        (32, 2, 128, 0, (8192, 1024)), (8, 1, 64, 0, (32768, 2048)),
+                                                        (32, 8, 128, 3, (8192, 1024))])
+def test_mixed_step_cache_written_bitwise(cpe, h_q, h_kv, d, n_decode, long_seq):
+    """cpe_mixed_step writes the round's K/V rows into the cache exactly as the
+    append does.  On a long launch (a long sequence in the batch) the extend
+    launch reads the chunk's keys from the new rows and writes the full new
+    pages of sequences whose prefix ends on a page boundary from its staged
+    tiles, the prep launch appending the rest; on a short one the prep launch
+    appends every row.  Cache bitwise against the oracle's append, output
+    against the oracle; page-aligned and unaligned prefixes, chunk lengths
+    with and without a partial last page, G = 4, 16, 8, decode rows beside."""
+    lens = [(L - 1, 1) for L in (40, 1, 2049)][:n_decode] + \
+        [(0, 45), (32, 300), (17, 100), (512, 128), (100, 7), (2048, 700), (160, 16)] + ([long_seq] if long_seq else [])
+    b = varlen_batch(80 + h_kv + n_decode + (1 if long_seq else 0), lens, h_q, h_kv, d)
+    kc_ref, vc_ref = b["k_cache"].cpu().clone(), b["v_cache"].cpu().clone()
+    oracle.kv_append(b["k_new"].cpu(), b["v_new"].cpu(), kc_ref, vc_ref, b["page_table_host"], b["qo"], b["pl"])
+    lse = torch.empty(b["q"].shape[0], h_q, dtype=torch.float32, device="cuda")
+    out, _ = cpe.cpe_mixed_step(b["q"], b["k_new"], b["v_new"], b["k_cache"], b["v_cache"], b["page_table"],
+                                i32(b["qo"]), i32(b["pl"]), n_decode, b["max_kv"], lse=lse)
+    _status_ok(cpe)
+    assert torch.equal(b["k_cache"].cpu(), kc_ref) and torch.equal(b["v_cache"].cpu(), vc_ref)
+    ref_o, ref_l = oracle.extend_attention(b["q"].cpu(), kc_ref, vc_ref, b["page_table_host"], b["qo"], b["pl"],
+                                           h_q, h_kv)
+    check_close(out, ref_o, f"mixed step {h_q}/{h_kv} d={d} decode={n_decode} long={long_seq}")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=LSE_ABS, rtol=0)
+
+
 # ---------------------------------------------------------------- extend, small, full compare
 
 SMALL = [
