@@ -303,9 +303,10 @@ cpe_status run_extend(const char* fn, const Common& c, int seq_begin, int row_be
   // With the round's new rows at hand, a long extend launch reads the chunk's
   // keys from them and writes the full new pages of page-aligned sequences
   // into the cache itself; the prep launch appends the rest.  (On short
-  // launches the stores' share of the time measured a few percent slower than
-  // the prep launch's append, so there the prep launch appends every row.)
-  const bool staged = append != nullptr && !dependent;
+  // launches, and beside the decode rows of a fused mixed step, the stores'
+  // share of the time measured slower than the prep launch's append, so there
+  // the prep launch appends every row.)
+  const bool staged = append != nullptr && !dependent && dec_rows == 0;
   KvAppendArgs ka{};
   if (append) {
     ka = *append;

@@ -90,17 +90,11 @@ struct TcCfg {
   static constexpr int kSmem = kBarOff + 512 + 1024;  // + barriers + alignment slack
 };
 
-// Ring slots are released per key tile: one commit after a key tile's MMAs
-// arrives on rel[r % NR] (r counts key tiles over the CTA's items) and frees
-// V_r and every K tile whose S products were issued by then.  NR exceeds both
-// ring depths, so a producer waiting on a release cannot miss its phase.
 template <int NK, int NV>
 struct Bars {
-  static constexpr int NR = (NK > NV ? NK : NV) + 1;
   uint64_t q_full, q_empty;
-  uint64_t k_full[NK];
-  uint64_t v_full[NV];
-  uint64_t rel[NR];
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
   // cache-page stores owed from each slot's current tile (kept by the slot's
   // producer): pages mask, sequence, key tile, KV head
   int k_owed[NK][4], v_owed[NV][4];
@@ -196,7 +190,11 @@ __device__ void decode_worker(const ExtendTcArgs& a, uint8_t* smem) {
   }
 }
 
-template <int D>
+// S (staged): the launch reads the chunk's keys from the round's new rows and
+// writes the full new pages of page-aligned sequences to the cache (long
+// launches with new rows at hand); a separate instantiation keeps the
+// producers of every other launch free of that work.
+template <int D, bool S>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendTcArgs a) {
   using C = TcCfg<D>;
   constexpr int NK = C::kStagesK;
@@ -235,9 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int i = 0; i < NK; ++i) mbar_init(&bars->k_full[i], 1);
-    for (int i = 0; i < NV; ++i) mbar_init(&bars->v_full[i], 1);
-    for (int i = 0; i < Bars<NK, NV>::NR; ++i) mbar_init(&bars->rel[i], 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
     for (int i = 0; i < NK; ++i) bars->k_owed[i][0] = 0;
     for (int i = 0; i < NV; ++i) bars->v_owed[i][0] = 0;
     for (int i = 0; i < 2; ++i) {
@@ -264,19 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const CUtensorMap* tmn128 = is_k ? &a.tm_kn128 : &a.tm_vn128;
       const int ns = is_k ? NK : NV;
       uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       uint8_t* ring = smem + (is_k ? C::kKOff : C::kVOff);
       prefetch_tmap(tm);
       prefetch_tmap(tm128);
-      if (a.staged) {
+      if constexpr (S) {
         prefetch_tmap(tmn);
         prefetch_tmap(tmn128);
       }
       if (is_k) prefetch_tmap(&a.tm_q);
       const int oob = static_cast<int>(a.num_pages * kPage);  // a row past the cache: zero fill
-      constexpr int NR = Bars<NK, NV>::NR;
-      int cnt = 0;       // ring loads issued so far (= key tiles, over the CTA's items)
+      int cnt = 0;       // ring loads issued so far
       int items = 0;     // Q loads issued so far
-      uint32_t firsts = 0;  // bit i: load cnt - 1 - i was the first key tile of its item
       int (*owed)[4] = is_k ? bars->k_owed : bars->v_owed;
       // The full new pages of a page-aligned sequence's own tokens are written
       // to the cache from the slot they were staged in, when the slot is
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         // the round's new rows, and the full pages of this unit's own tokens
         // (keys P + [2 pair tok, 2 pair tok + 2 tok)) are written to the cache
         // from the staged tile.  Otherwise everything comes from the cache.
-        const bool staged = a.staged && it.P % kPage == 0;
+        const bool staged = S && it.P % kPage == 0;
         for (int j = it.kv_lo; j < it.kv_hi; ++j, ++cnt) {
           const int st = cnt % ns;
           const int use = cnt / ns;
@@ -341,23 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
               contiguous = contiguous && rows[pg] == rows[0] + pg * kPage;
             }
           }
-          // The load this one replaces, m = cnt - ns, was released with key
-          // tile m's MMAs; a K tile whose S products were issued one key tile
-          // earlier (every K tile but an item's first) already with key tile m - 1.
-          if (use > 0) {
-            const int m = cnt - ns;
-            const int r = (is_k && !((firsts >> (ns - 1)) & 1u)) ? m - 1 : m;
-            if (!mbar_wait(&bars->rel[r % NR], (r / NR) & 1, abort, a.wait_ns, a.status,
-                           is_k ? kDetailKEmpty : kDetailVEmpty)) {
-              ok = false;
-              break;
-            }
+          if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, abort, a.wait_ns, a.status,
+                                    is_k ? kDetailKEmpty : kDetailVEmpty)) {
+            ok = false;
+            break;
           }
-          if (a.staged && owed[st][0]) {  // the slot's previous tile owes cache pages: store them, let them read the slot
+          if (S && owed[st][0]) {  // the slot's previous tile owes cache pages: store them, let them read the slot
             store_owed(st);
             bulk_wait_read_all();
           }
-          if (staged) {
+          if (S && staged) {
             const uint32_t own = own_pages(it, a.tok, kb, pnew, npg);
             if (own) {
               owed[st][0] = static_cast<int>(own);
@@ -366,16 +361,22 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
               owed[st][3] = it.g;
             }
           }
-          firsts = (firsts << 1) | (j == it.kv_lo ? 1u : 0u);
           uint8_t* dst = ring + st * C::kTileBytes;
           mbar_arrive_expect_tx(&full[st], npg * C::kHalves * (kPage * 128));
           if (contiguous) {
             for (int h = 0; h < C::kHalves; ++h)
               tma_load_3d(dst + h * C::kHalfBytes, tm128, &full[st], h * 64, it.g, rows[0]);
+          } else if (!S) {
+#pragma unroll
+            for (int pg = 0; pg < kBlockN / kPage; ++pg) {
+              if (pg >= npg) break;
+              for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(dst + h * C::kHalfBytes + pg * (kPage * 128), tm, &full[st], h * 64, it.g, rows[pg]);
+            }
           } else if (pnew == 0 && npg == kBlockN / kPage) {  // eight new pages: rows q0 + kb - P onwards
             for (int h = 0; h < C::kHalves; ++h)
               tma_load_3d(dst + h * C::kHalfBytes, tmn128, &full[st], h * 64, it.g, it.q0 + kb - it.P);
-          } else {
+          } else {  // cached pages below P, new rows from P on
 #pragma unroll
             for (int pg = 0; pg < kBlockN / kPage; ++pg) {
               if (pg >= npg) break;
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (is_k && items > 0) mbar_wait(&bars->q_full, (items - 1) & 1, no_abort, kDrainNs, a.status, kDetailDrain);
         for (int n = max(0, cnt - ns); n < cnt; ++n)
           mbar_wait(&full[n % ns], (n / ns) & 1, no_abort, kDrainNs, a.status, kDetailDrain);
-      } else if (a.staged) {
+      } else if (S) {
         // the last tiles' owed pages, once each has landed
         for (int n = max(0, cnt - ns); n < cnt; ++n) {
           if (!owed[n % ns][0]) continue;
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           store_owed(n % ns);
         }
       }
-      if (a.staged) bulk_wait_read_all();  // no store still reads the ring when the CTA leaves
+      if constexpr (S) bulk_wait_read_all();  // no store still reads the ring when the CTA leaves
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
@@ -418,7 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_commit(&bars->s_full[t]);
       };
       int kc = 0, vc = 0, items = 0;
-      int rs = 0;  // release barrier of the next key tile
       int pc0 = 0, pc1 = 0;  // P hand-offs consumed per tile
       bool ok = true;
       Item it;
@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         tc_fence_after();
         if (it.kv_lo < it.n_kt_0) issue_s(0, kc % NK);
         if (it.kv_lo < it.n_kt_1) issue_s(1, kc % NK);
+        tc_commit(&bars->k_empty[kc % NK]);
         ++kc;
         for (int j = it.kv_lo; j < it.kv_hi; ++j) {
           // Both operand stages this key tile needs are waited for up front, so
@@ -490,11 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             ok = false;
             break;
           }
-          // one release per key tile: V_j, and K_{j+1} (and K_j at an item's start)
-          tc_commit(&bars->rel[rs]);
-          rs = rs + 1 == Bars<NK, NV>::NR ? 0 : rs + 1;
+          tc_commit(&bars->v_empty[sv_st]);
           ++vc;
-          if (more) ++kc;
+          if (more) {
+            tc_commit(&bars->k_empty[kc % NK]);
+            ++kc;
+          }
         }
         tc_commit(&bars->q_empty);  // every S of this item issued: Q may be replaced
       }
@@ -1246,10 +1248,10 @@ size_t extend_tc_smem_bytes(int d) {
 
 // The softmax warpgroups raise their register limit at run time; that only
 // completes if the launch allocated at least kLaunchRegs per thread.
-template <int D>
+template <int D, bool S>
 cudaError_t check_regs() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, extend_tc_kernel<D>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, extend_tc_kernel<D, S>);
   if (e != cudaSuccess) return e;
   return fa.numRegs >= kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
@@ -1291,39 +1293,39 @@ cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream
   return cudaLaunchKernelEx(&cfg, prep_kernel, a, k);
 }
 
-// Once per device and head size: the register check and the shared-memory
-// opt-in (both hold for the loaded module).
-template <int D>
+// Once per device, head size and form: the register check and the
+// shared-memory opt-in (both hold for the loaded module).
+template <int D, bool S>
 cudaError_t prepare_extend() {
   static std::atomic<int> ready[64];  // 0: not yet, 1: done
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && ready[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = check_regs<D>();
+  e = check_regs<D, S>();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(extend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
+  e = cudaFuncSetAttribute(extend_tc_kernel<D, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
   return cudaSuccess;
 }
 
-cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
-  if (a.n_ctas <= 0) return cudaSuccess;
-  cudaError_t e = a.d == 128 ? prepare_extend<128>() : prepare_extend<64>();
+template <int D, bool S>
+cudaError_t launch_extend_form(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
+  cudaError_t e = prepare_extend<D, S>();
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(extend_tc_kernel<D, S>, a.n_ctas, kThreads, TcCfg<D>::kSmem, s, a, dependent);
   if (e != cudaSuccess) return e;
   // the merge's persistent grid: two blocks per SM, fewer if there cannot be that much work
   const int merge_grid = std::max(1, std::min(a.max_split * kMergeRowGroups, 2 * a.n_ctas));
-  if (a.d == 128) {
-    e = launch_dependent(extend_tc_kernel<128>, a.n_ctas, kThreads, TcCfg<128>::kSmem, s, a, dependent);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(extend_merge_kernel<128>, merge_grid, kMergeThreads, 0, s, a, dependent);
-  } else {
-    e = launch_dependent(extend_tc_kernel<64>, a.n_ctas, kThreads, TcCfg<64>::kSmem, s, a, dependent);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(extend_merge_kernel<64>, merge_grid, kMergeThreads, 0, s, a, dependent);
-  }
-  return e;
+  return launch_dependent(extend_merge_kernel<D>, merge_grid, kMergeThreads, 0, s, a, dependent);
+}
+
+cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
+  if (a.n_ctas <= 0) return cudaSuccess;
+  if (a.d == 128)
+    return a.staged ? launch_extend_form<128, true>(a, s, dependent) : launch_extend_form<128, false>(a, s, dependent);
+  return a.staged ? launch_extend_form<64, true>(a, s, dependent) : launch_extend_form<64, false>(a, s, dependent);
 }
 
 }  // namespace cpe
