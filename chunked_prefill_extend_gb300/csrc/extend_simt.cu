@@ -1,7 +1,9 @@
 // Extend attention on CUDA cores in fp32 arithmetic: the path for fp32 data
 // (exact fp32 inputs, no tensor-core rounding).  One warp per (query row,
-// head); each lane holds d/32 dimensions of q, keys are visited one at a time
-// with a warp-reduced dot product and a running (m, l, o).
+// head), keys in blocks of 32: each lane scores one key of the block against
+// the whole query row, the warp takes the block's max and sum for the running
+// (m, l), and each lane accumulates d/32 output dimensions over the block's
+// weighted values.
 #include "cpe_device.cuh"
 #include "kernels.h"
 
@@ -29,6 +31,7 @@ __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16* p, int64_t i, f
 
 template <typename T, int DPL>  // DPL = d / 32 dimensions per lane
 __global__ void __launch_bounds__(128) extend_simt_kernel(ExtendSimtArgs a) {
+  constexpr int D = 32 * DPL;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int n_rows = a.total_q - a.row_begin;
@@ -52,36 +55,69 @@ __global__ void __launch_bounds__(128) extend_simt_kernel(ExtendSimtArgs a) {
   const T* q = static_cast<const T*>(a.q);
   const T* kc = static_cast<const T*>(a.k_cache);
   const T* vc = static_cast<const T*>(a.v_cache);
-  float qr[DPL], o[DPL];
-  const int64_t qoff = (static_cast<int64_t>(row) * a.h_q + h) * a.d;
+  // every lane holds the whole query row (for its key's dot product) and
+  // DPL output dimensions
+  float qr[D], o[DPL];
+  const int64_t qoff = (static_cast<int64_t>(row) * a.h_q + h) * D;
 #pragma unroll
-  for (int x = 0; x < DPL; ++x) {
-    qr[x] = ld(q, qoff + lane * DPL + x);
-    o[x] = 0.f;
-  }
+  for (int x = 0; x < D; ++x) qr[x] = ld(q, qoff + x);
+#pragma unroll
+  for (int x = 0; x < DPL; ++x) o[x] = 0.f;
   float m = -INFINITY, l = 0.f;
   const int32_t* pt = a.page_table + static_cast<int64_t>(s) * a.max_pages;
   const int last = P + i;
-  for (int j = 0; j <= last; ++j) {
-    const int pid = pt[j / a.page_size];
-    if (pid < 0 || pid >= a.num_pages) {
-      if (lane == 0) record_error(a.status, kStatusDeviceArg, kDetailBadPage);
-      return;
+  // Keys in blocks of 32, lane j scoring key kb + j: one warp max and sum per
+  // block for the running (m, l), then the block's weighted values.
+  for (int kb = 0; kb <= last; kb += 32) {
+    const int j = kb + lane;
+    int64_t krow = 0;
+    float sc = -INFINITY;
+    if (j <= last) {
+      const int pid = pt[j / a.page_size];
+      if (pid < 0 || pid >= a.num_pages) {
+        record_error(a.status, kStatusDeviceArg, kDetailBadPage);
+      } else {
+        krow = ((static_cast<int64_t>(pid) * a.page_size + j % a.page_size) * a.h_kv + g) * D;
+        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (sizeof(T) == 4) {  // the key row in 16-byte vectors
+          const float4* kr = reinterpret_cast<const float4*>(kc + krow);
+#pragma unroll
+          for (int x = 0; x < D / 4; ++x) {
+            const float4 k4 = __ldg(kr + x);
+            dot[0] = fmaf(qr[4 * x], k4.x, dot[0]);
+            dot[1] = fmaf(qr[4 * x + 1], k4.y, dot[1]);
+            dot[2] = fmaf(qr[4 * x + 2], k4.z, dot[2]);
+            dot[3] = fmaf(qr[4 * x + 3], k4.w, dot[3]);
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < D; ++x) dot[x & 3] = fmaf(qr[x], ld(kc, krow + x), dot[x & 3]);
+        }
+        sc = ((dot[0] + dot[1]) + (dot[2] + dot[3])) * a.sm_scale;
+      }
     }
-    const int64_t koff = ((static_cast<int64_t>(pid) * a.page_size + j % a.page_size) * a.h_kv + g) * a.d +
-                         lane * DPL;
-    float dot = 0.f;
+    float mb = sc;
 #pragma unroll
-    for (int x = 0; x < DPL; ++x) dot = fmaf(qr[x], ld(kc, koff + x), dot);
+    for (int o2 = 16; o2 > 0; o2 >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o2));
+    const float m_new = fmaxf(m, mb);
+    const float corr = m == -INFINITY ? 0.f : expf(m - m_new);
+    const float p = sc == -INFINITY ? 0.f : expf(sc - m_new);
+    float ps = p;
 #pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o2);
-    const float sc = dot * a.sm_scale;
-    const float m_new = fmaxf(m, sc);
-    const float corr = expf(m - m_new);
-    const float p = expf(sc - m_new);
-    l = l * corr + p;
+    for (int o2 = 16; o2 > 0; o2 >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o2);
+    l = l * corr + ps;
 #pragma unroll
-    for (int x = 0; x < DPL; ++x) o[x] = fmaf(o[x], corr, p * ld(vc, koff + x));
+    for (int x = 0; x < DPL; ++x) o[x] *= corr;
+    const int nk = min(32, last + 1 - kb);
+#pragma unroll 8
+    for (int jj = 0; jj < 32; ++jj) {  // (keys past the last have p = 0 and row 0: skipped)
+      if (jj < nk) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+        const int64_t vrow = __shfl_sync(0xffffffffu, krow, jj);
+#pragma unroll
+        for (int x = 0; x < DPL; ++x) o[x] = fmaf(pj, ld(vc, vrow + lane * DPL + x), o[x]);
+      }
+    }
     m = m_new;
   }
   T* out = static_cast<T*>(a.out);
