@@ -435,6 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (it.kv_lo < it.n_kt_1) issue_s(1, kc % NK);
         tc_commit(&bars->k_empty[kc % NK]);
         ++kc;
+        // Q is released once the item's last S is issued (here for a one-tile
+        // item, else in the loop at its second-last key tile), so the next
+        // item's Q load overlaps the last tile's softmax and P.V.  The staged
+        // form releases it after the item: there the producer's refill of the
+        // last tiles' slots stores their owed pages, and those stores, moved
+        // under the last P.V bursts, measured slower (long rounds -0.7 %).
+        if (!S && it.kv_lo + 1 == it.kv_hi) tc_commit(&bars->q_empty);
         for (int j = it.kv_lo; j < it.kv_hi; ++j) {
           // Both operand stages this key tile needs are waited for up front, so
           // the MMA bursts below are separated only by the softmax hand-offs.
@@ -497,8 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             tc_commit(&bars->k_empty[kc % NK]);
             ++kc;
           }
+          // every S of the item issued (the last at key tile kv_hi - 2, for
+          // the query tile with the most key tiles): Q may be replaced
+          if (!S && j + 2 == it.kv_hi) tc_commit(&bars->q_empty);
         }
-        tc_commit(&bars->q_empty);  // every S of this item issued: Q may be replaced
+        if (S) tc_commit(&bars->q_empty);
       }
       // Drain: wait until every MMA issued above has completed.
       tc_commit(&bars->drain);
