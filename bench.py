@@ -32,6 +32,10 @@ import time
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+# The fp32 path's roofline: FP32 FMA lanes per SM and the maximum SM clock of
+# a GB300 (the peak is SMs x lanes x 2 flop x clock)
+FP32_LANES_PER_SM = 128
+FP32_PEAK_CLOCK_MHZ = 2070
 sys.path.insert(0, ROOT)
 
 from chunked_prefill_extend_gb300 import workloads as W  # noqa: E402
@@ -605,14 +609,17 @@ def measure(wl, name, steps, warmup, peaks, ws, device, traffic_ok=False):
         per_launch = wl.flops / nch
         achieved = per_launch / (kms * 1e-3) / 1e12
         if wl.spec.dtype == torch.bfloat16:
-            pk, src = peaks["bf16_sustained"], peaks["source"] + " bf16_tflops_sustained"
-        else:  # tf32 tensor cores: half the bf16 rate per the nominal dense figures (1.1 vs 2.25 PFLOP/s)
-            pk, src = peaks["bf16_sustained"] / 2, peaks["source"] + " bf16_tflops_sustained x 1/2 (tf32)"
+            bound, pk, src = "tensor", peaks["bf16_sustained"], peaks["source"] + " bf16_tflops_sustained"
+            kname = "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)"
+        else:  # fp32 data runs on the CUDA cores: FP32 FMA issue rate, SMs x 128 lanes x 2 flop x clock
+            n_sms = torch.cuda.get_device_properties(device).multi_processor_count
+            bound, pk = "alu", FP32_LANES_PER_SM * 2 * n_sms * FP32_PEAK_CLOCK_MHZ * 1e6 / 1e12
+            src = (f"derived: {n_sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop (FMA) x "
+                   f"{FP32_PEAK_CLOCK_MHZ} MHz (maximum SM clock)")
+            kname = "one round's call: K/V append + extend attention (kv_append_kernel + extend_simt_kernel, fp32)"
         traffic = profiled_traffic(per_launch) if traffic_ok else None
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
-                "traffic": traffic,
-                "kernel": "one round's call: K/V append + extend attention (prep_kernel + extend_tc_kernel + merge)",
-                "peak_source": src, "units_per_launch": per_launch}
+        roof = {"bound": bound, "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "traffic": traffic, "kernel": kname, "peak_source": src, "units_per_launch": per_launch}
         # per round: a pass after the timed region with events around every
         # call (so each call runs alone); the median over its steps
         kev = ([], [])
