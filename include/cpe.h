@@ -32,6 +32,10 @@
  *      k/v cache    [num_pages, page_size, H_kv, d]
  *      page_table   [n_seqs, max_pages] int32 (page ids; entries past a
  *                   sequence's last page are never read)
+ *    Cache slots past a sequence's last token in its last page must hold
+ *    finite values (zero-initialised pages do): the tensor-core path loads
+ *    whole 16-token steps and meets them with zero weights, and 0 x (inf or
+ *    NaN) is NaN.
  *      qo_indptr    [n_seqs + 1] int32, qo_indptr[0] = 0, non-decreasing,
  *                   qo_indptr[n_seqs] = total_q
  *      prefix_len   [n_seqs] int32
