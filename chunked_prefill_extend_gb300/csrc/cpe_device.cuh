@@ -146,6 +146,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns, int* status, int detail);
+
+// mbar_wait after up to `polls` non-blocking tests: for a thread with nothing
+// else to do whose wake-up latency matters more than the issue slots its
+// polls take from the warps beside it.
+__device__ __forceinline__ bool mbar_wait_polled(uint64_t* bar, uint32_t parity, int polls, volatile int* abort,
+                                                 uint64_t limit_ns, int* status, int detail) {
+#pragma unroll 1
+  for (int i = 0; i < polls; ++i)
+    if (mbar_test(bar, parity)) return true;
+  return mbar_wait(bar, parity, abort, limit_ns, status, detail);
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up when
 // `*abort` becomes non-zero or after `limit_ns` nanoseconds: then it records a
 // timeout in the status word, raises the CTA's abort flag and returns false.

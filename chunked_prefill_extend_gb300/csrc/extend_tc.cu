@@ -70,6 +70,7 @@ namespace cpe {
 namespace {
 
 constexpr int kThreads = 384;
+constexpr int kRefillPolls = 64;     // staged form: slot polls before a producer's suspending wait
 constexpr int kLaunchRegs = 168;     // 384 x 168 = 64512 registers at launch
 constexpr int kProducerRegs = 96;    // warpgroup 0 after setmaxnreg.dec
 constexpr int kSoftmaxRegs = 200;    // warpgroups 1, 2 after setmaxnreg.inc
@@ -343,8 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
               contiguous = contiguous && rows[pg] == rows[0] + pg * kPage;
             }
           }
-          if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, abort, a.wait_ns, a.status,
-                                    is_k ? kDetailKEmpty : kDetailVEmpty)) {
+          // (the staged form polls the slot first: measured faster on its long
+          // launches; on fused mixed steps the polls slowed the softmax warps)
+          if (use > 0 && !mbar_wait_polled(&empty[st], (use - 1) & 1, S ? kRefillPolls : 0, abort, a.wait_ns,
+                                           a.status, is_k ? kDetailKEmpty : kDetailVEmpty)) {
             ok = false;
             break;
           }
