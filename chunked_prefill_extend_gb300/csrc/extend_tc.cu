@@ -193,9 +193,11 @@ __device__ void decode_worker(const ExtendTcArgs& a, uint8_t* smem) {
 
 // S (staged): the launch reads the chunk's keys from the round's new rows and
 // writes the full new pages of page-aligned sequences to the cache (long
-// launches with new rows at hand); a separate instantiation keeps the
-// producers of every other launch free of that work.
-template <int D, bool S>
+// launches with new rows at hand).  F (fused): decode rows share the launch
+// (a fused mixed step).  Separate instantiations keep the code of every other
+// launch free of that work: three forms per head size, plain, staged and
+// fused.
+template <int D, bool S, bool F>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendTcArgs a) {
   using C = TcCfg<D>;
   constexpr int NK = C::kStagesK;
@@ -369,6 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           if (contiguous) {
             for (int h = 0; h < C::kHalves; ++h)
               tma_load_3d(dst + h * C::kHalfBytes, tm128, &full[st], h * 64, it.g, rows[0]);
+            // Beside decode rows (a fused mixed step) the HBM is saturated and
+            // a copy's latency grows: the tile two ahead is prefetched into L2,
+            // on the guess that the pages stay consecutive (a wrong guess only
+            // wastes the prefetch).  Elsewhere the CTAs that stream a KV
+            // head's keys together already serve each other from L2, and the
+            // prefetches measured slower.
+            if (F && j + 2 < it.kv_hi && rows[0] + 3 * kBlockN <= oob)
+              for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(tm128, h * 64, it.g, rows[0] + 2 * kBlockN);
           } else if (!S) {
 #pragma unroll
             for (int pg = 0; pg < kBlockN / kPage; ++pg) {
@@ -1261,10 +1271,10 @@ size_t extend_tc_smem_bytes(int d) {
 
 // The softmax warpgroups raise their register limit at run time; that only
 // completes if the launch allocated at least kLaunchRegs per thread.
-template <int D, bool S>
+template <int D, bool S, bool F>
 cudaError_t check_regs() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, extend_tc_kernel<D, S>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, extend_tc_kernel<D, S, F>);
   if (e != cudaSuccess) return e;
   return fa.numRegs >= kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
@@ -1308,26 +1318,26 @@ cudaError_t launch_prep(const ScheduleArgs& a, const KvAppendArgs& k, cudaStream
 
 // Once per device, head size and form: the register check and the
 // shared-memory opt-in (both hold for the loaded module).
-template <int D, bool S>
+template <int D, bool S, bool F>
 cudaError_t prepare_extend() {
   static std::atomic<int> ready[64];  // 0: not yet, 1: done
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && ready[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = check_regs<D, S>();
+  e = check_regs<D, S, F>();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(extend_tc_kernel<D, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
+  e = cudaFuncSetAttribute(extend_tc_kernel<D, S, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
   return cudaSuccess;
 }
 
-template <int D, bool S>
+template <int D, bool S, bool F>
 cudaError_t launch_extend_form(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
-  cudaError_t e = prepare_extend<D, S>();
+  cudaError_t e = prepare_extend<D, S, F>();
   if (e != cudaSuccess) return e;
-  e = launch_dependent(extend_tc_kernel<D, S>, a.n_ctas, kThreads, TcCfg<D>::kSmem, s, a, dependent);
+  e = launch_dependent(extend_tc_kernel<D, S, F>, a.n_ctas, kThreads, TcCfg<D>::kSmem, s, a, dependent);
   if (e != cudaSuccess) return e;
   // the merge's persistent grid: two blocks per SM, fewer if there cannot be that much work
   const int merge_grid = std::max(1, std::min(a.max_split * kMergeRowGroups, 2 * a.n_ctas));
@@ -1336,9 +1346,15 @@ cudaError_t launch_extend_form(const ExtendTcArgs& a, cudaStream_t s, bool depen
 
 cudaError_t launch_extend_tc(const ExtendTcArgs& a, cudaStream_t s, bool dependent) {
   if (a.n_ctas <= 0) return cudaSuccess;
-  if (a.d == 128)
-    return a.staged ? launch_extend_form<128, true>(a, s, dependent) : launch_extend_form<128, false>(a, s, dependent);
-  return a.staged ? launch_extend_form<64, true>(a, s, dependent) : launch_extend_form<64, false>(a, s, dependent);
+  // (the staged form never carries decode rows: the host stages only launches without them)
+  if (a.d == 128) {
+    if (a.staged) return launch_extend_form<128, true, false>(a, s, dependent);
+    return a.dec_items > 0 ? launch_extend_form<128, false, true>(a, s, dependent)
+                           : launch_extend_form<128, false, false>(a, s, dependent);
+  }
+  if (a.staged) return launch_extend_form<64, true, false>(a, s, dependent);
+  return a.dec_items > 0 ? launch_extend_form<64, false, true>(a, s, dependent)
+                         : launch_extend_form<64, false, false>(a, s, dependent);
 }
 
 }  // namespace cpe
